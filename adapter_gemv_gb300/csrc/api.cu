@@ -1,0 +1,272 @@
+// api.cu -- the C ABI of libmlora (declared in include/mlora.h).
+//
+// Host side only: argument validation (every host-detectable error is returned before any
+// launch), translation of the public structs into kernel parameter blocks, and dispatch to
+// the kernels. Nothing here allocates device memory or synchronises the host.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "launch.h"
+#include "mlora.h"
+
+namespace {
+
+thread_local char g_cuda_err[256] = "no CUDA error recorded";
+std::atomic<int64_t> g_launches{0};
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int cuda_fail(cudaError_t e, const char *where) {
+  snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+  return MLORA_ERR_CUDA;
+}
+
+// Checks a pool descriptor for the phases a call runs.
+int check_pool(const mlora_pool *p, int32_t layer, bool need_a, bool need_b) {
+  if (!p) return MLORA_ERR_NULL;
+  if (p->dtype != MLORA_BF16 && p->dtype != MLORA_FP16) return MLORA_ERR_DTYPE;
+  if (!p->rank || !p->scale) return MLORA_ERR_NULL;
+  if (p->num_slots < 1 || p->num_layers < 1 || p->r_max < 1 || p->r_max > MLORA_MAX_RANK) return MLORA_ERR_SHAPE;
+  if (p->d_in < 8 || p->d_out < 8) return MLORA_ERR_SHAPE;
+  if (p->d_in % 8 || p->d_out % 8) return MLORA_ERR_ALIGN;
+  if (layer < 0 || layer >= p->num_layers) return MLORA_ERR_SHAPE;
+  if (!aligned(p->rank, 4) || !aligned(p->scale, 4)) return MLORA_ERR_ALIGN;
+  if (p->kind == MLORA_POOL_STACKED) {
+    if ((need_a && !p->a_t) || (need_b && !p->b)) return MLORA_ERR_NULL;
+    if ((need_a && !aligned(p->a_t, 16)) || (need_b && !aligned(p->b, 16))) return MLORA_ERR_ALIGN;
+  } else if (p->kind == MLORA_POOL_PAGED) {
+    if (!p->pages || (need_a && !p->a_page_table) || (need_b && !p->b_page_table)) return MLORA_ERR_NULL;
+    if (p->num_pages < 1 || p->page_elems < (need_a ? p->d_in : 0) || p->page_elems < (need_b ? p->d_out : 0))
+      return MLORA_ERR_POOL;
+    if (p->num_pages > INT32_MAX) return MLORA_ERR_POOL;  // page ids are int32
+    if (!aligned(p->pages, 16) || p->page_elems % 8) return MLORA_ERR_ALIGN;
+    if ((need_a && !aligned(p->a_page_table, 4)) || (need_b && !aligned(p->b_page_table, 4))) return MLORA_ERR_ALIGN;
+  } else {
+    return MLORA_ERR_POOL;
+  }
+  return MLORA_OK;
+}
+
+mlora::PoolDev to_dev(const mlora_pool *p) {
+  mlora::PoolDev d{};
+  d.kind = p->kind;
+  d.dtype = p->dtype;
+  d.num_slots = p->num_slots;
+  d.num_layers = p->num_layers;
+  d.r_max = p->r_max;
+  d.d_in = p->d_in;
+  d.d_out = p->d_out;
+  d.a_t = static_cast<const uint16_t *>(p->a_t);
+  d.b = static_cast<const uint16_t *>(p->b);
+  d.pages = static_cast<const uint16_t *>(p->pages);
+  d.page_elems = p->page_elems;
+  d.num_pages = p->num_pages;
+  d.a_tab = p->a_page_table;
+  d.b_tab = p->b_page_table;
+  d.rank = p->rank;
+  d.scale = p->scale;
+  return d;
+}
+
+int check_x(const void *x, int64_t ldx, const mlora_pool *p) {
+  if (!x) return MLORA_ERR_NULL;
+  if (ldx < p->d_in) return MLORA_ERR_SHAPE;
+  if (!aligned(x, 16) || ldx % 8) return MLORA_ERR_ALIGN;
+  return MLORA_OK;
+}
+
+int check_y(const void *y, int64_t ldy, const mlora_pool *p) {
+  if (!y) return MLORA_ERR_NULL;
+  if (ldy < p->d_out) return MLORA_ERR_SHAPE;
+  if (!aligned(y, 16) || ldy % 8) return MLORA_ERR_ALIGN;
+  return MLORA_OK;
+}
+
+int check_v(const float *v) {
+  if (!v) return MLORA_ERR_NULL;
+  if (!aligned(v, 4)) return MLORA_ERR_ALIGN;
+  return MLORA_OK;
+}
+
+int check_rows_sgmv(const int32_t *off, const int32_t *slot, int32_t nseg, int32_t num_rows, const int32_t *status) {
+  if (num_rows < 0 || nseg < 0) return MLORA_ERR_SHAPE;
+  if (!off || (nseg > 0 && !slot)) return MLORA_ERR_NULL;
+  if (!aligned(off, 4) || !aligned(slot, 4) || !aligned(status, 4)) return MLORA_ERR_ALIGN;
+  return MLORA_OK;
+}
+
+int check_rows_bgmv(const int32_t *row_slot, int32_t num_rows, const int32_t *status) {
+  if (num_rows < 0) return MLORA_ERR_SHAPE;
+  if (num_rows > 0 && !row_slot) return MLORA_ERR_NULL;
+  if (!aligned(row_slot, 4) || !aligned(status, 4)) return MLORA_ERR_ALIGN;
+  return MLORA_OK;
+}
+
+#define TRY(expr)              \
+  do {                         \
+    const int rc_ = (expr);    \
+    if (rc_ != MLORA_OK) return rc_; \
+  } while (0)
+
+mlora::DecodeParams base_params(const int32_t *off, const int32_t *seg_slot, int32_t nseg, const int32_t *row_slot,
+                                int32_t num_rows, int32_t *status) {
+  mlora::DecodeParams d{};
+  d.seg_off = off;
+  d.seg_slot = seg_slot;
+  d.nseg = nseg;
+  d.row_slot = row_slot;
+  d.M = num_rows;
+  d.status = status;
+  return d;
+}
+
+int run(int mode, int dtype, const mlora::DecodeParams &d, void *stream) {
+  const cudaError_t e = mlora::launch_decode(mode, dtype, d, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return MLORA_OK;
+}
+
+mlora::ProblemDev problem(const mlora_pool *pool, int32_t layer, const void *x, int64_t ldx, void *y, int64_t ldy,
+                          float *v) {
+  mlora::ProblemDev q{};
+  q.pool = to_dev(pool);
+  q.layer = layer;
+  q.x = static_cast<const uint16_t *>(x);
+  q.ldx = ldx;
+  q.y = static_cast<uint16_t *>(y);
+  q.ldy = ldy;
+  q.v = v;
+  return q;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lora_sgmv_shrink(float *v, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *seg_offsets,
+                     const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t layer,
+                     int32_t *dev_status, void *stream) {
+  TRY(check_pool(pool, layer, true, false));
+  TRY(check_v(v));
+  TRY(check_x(x, ldx, pool));
+  TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
+  if (num_rows == 0) return MLORA_OK;
+  mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
+  d.prob[0] = problem(pool, layer, x, ldx, nullptr, 0, v);
+  d.nprob = 1;
+  return run(mlora::MODE_SHRINK, pool->dtype, d, stream);
+}
+
+int lora_sgmv_expand(void *y, int64_t ldy, const float *v, const mlora_pool *pool, const int32_t *seg_offsets,
+                     const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t layer,
+                     int32_t *dev_status, void *stream) {
+  TRY(check_pool(pool, layer, false, true));
+  TRY(check_v(v));
+  TRY(check_y(y, ldy, pool));
+  TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
+  if (num_rows == 0) return MLORA_OK;
+  mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
+  d.prob[0] = problem(pool, layer, nullptr, 0, y, ldy, const_cast<float *>(v));
+  d.nprob = 1;
+  return run(mlora::MODE_EXPAND, pool->dtype, d, stream);
+}
+
+int lora_bgmv_shrink(float *v, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
+                     int32_t num_rows, int32_t layer, int32_t *dev_status, void *stream) {
+  TRY(check_pool(pool, layer, true, false));
+  TRY(check_v(v));
+  TRY(check_x(x, ldx, pool));
+  TRY(check_rows_bgmv(row_slot, num_rows, dev_status));
+  if (num_rows == 0) return MLORA_OK;
+  mlora::DecodeParams d = base_params(nullptr, nullptr, 0, row_slot, num_rows, dev_status);
+  d.prob[0] = problem(pool, layer, x, ldx, nullptr, 0, v);
+  d.nprob = 1;
+  return run(mlora::MODE_SHRINK, pool->dtype, d, stream);
+}
+
+int lora_bgmv_expand(void *y, int64_t ldy, const float *v, const mlora_pool *pool, const int32_t *row_slot,
+                     int32_t num_rows, int32_t layer, int32_t *dev_status, void *stream) {
+  TRY(check_pool(pool, layer, false, true));
+  TRY(check_v(v));
+  TRY(check_y(y, ldy, pool));
+  TRY(check_rows_bgmv(row_slot, num_rows, dev_status));
+  if (num_rows == 0) return MLORA_OK;
+  mlora::DecodeParams d = base_params(nullptr, nullptr, 0, row_slot, num_rows, dev_status);
+  d.prob[0] = problem(pool, layer, nullptr, 0, y, ldy, const_cast<float *>(v));
+  d.nprob = 1;
+  return run(mlora::MODE_EXPAND, pool->dtype, d, stream);
+}
+
+int lora_sgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *seg_offsets,
+              const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t layer, float *v_scratch,
+              int32_t *dev_status, void *stream) {
+  TRY(check_pool(pool, layer, true, true));
+  TRY(check_v(v_scratch));
+  TRY(check_x(x, ldx, pool));
+  TRY(check_y(y, ldy, pool));
+  TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
+  if (num_rows == 0) return MLORA_OK;
+  mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
+  d.prob[0] = problem(pool, layer, x, ldx, y, ldy, v_scratch);
+  d.nprob = 1;
+  return run(mlora::MODE_FUSED, pool->dtype, d, stream);
+}
+
+int lora_bgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
+              int32_t num_rows, int32_t layer, float *v_scratch, int32_t *dev_status, void *stream) {
+  TRY(check_pool(pool, layer, true, true));
+  TRY(check_v(v_scratch));
+  TRY(check_x(x, ldx, pool));
+  TRY(check_y(y, ldy, pool));
+  TRY(check_rows_bgmv(row_slot, num_rows, dev_status));
+  if (num_rows == 0) return MLORA_OK;
+  mlora::DecodeParams d = base_params(nullptr, nullptr, 0, row_slot, num_rows, dev_status);
+  d.prob[0] = problem(pool, layer, x, ldx, y, ldy, v_scratch);
+  d.nprob = 1;
+  return run(mlora::MODE_FUSED, pool->dtype, d, stream);
+}
+
+int lora_sgmv_grouped(const mlora_problem *problems, int32_t num_problems, const int32_t *seg_offsets,
+                      const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t *dev_status,
+                      void *stream) {
+  if (!problems) return MLORA_ERR_NULL;
+  if (num_problems < 1 || num_problems > MLORA_MAX_GROUP) return MLORA_ERR_SHAPE;
+  TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
+  mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
+  for (int q = 0; q < num_problems; ++q) {
+    const mlora_problem &pb = problems[q];
+    TRY(check_pool(pb.pool, pb.layer, true, true));
+    if (pb.pool->dtype != problems[0].pool->dtype) return MLORA_ERR_DTYPE;
+    TRY(check_v(pb.v_scratch));
+    TRY(check_x(pb.x, pb.ldx, pb.pool));
+    TRY(check_y(pb.y, pb.ldy, pb.pool));
+    d.prob[q] = problem(pb.pool, pb.layer, pb.x, pb.ldx, pb.y, pb.ldy, pb.v_scratch);
+  }
+  d.nprob = num_problems;
+  if (num_rows == 0) return MLORA_OK;
+  return run(mlora::MODE_FUSED, problems[0].pool->dtype, d, stream);
+}
+
+const char *lora_error_string(int code) {
+  switch (code) {
+    case MLORA_OK: return "ok";
+    case MLORA_ERR_NULL: return "a required pointer is NULL";
+    case MLORA_ERR_DTYPE: return "unsupported or mismatched dtype";
+    case MLORA_ERR_SHAPE: return "a size or index is out of range";
+    case MLORA_ERR_ALIGN: return "alignment rule broken (16-byte pointers, multiples of 8 elements)";
+    case MLORA_ERR_POOL: return "malformed adapter pool descriptor";
+    case MLORA_ERR_CUDA: return g_cuda_err;
+    default: return "unknown error code";
+  }
+}
+
+int lora_abi_version(void) { return MLORA_ABI_VERSION; }
+
+int64_t lora_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

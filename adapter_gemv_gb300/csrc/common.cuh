@@ -1,0 +1,171 @@
+// common.cuh -- device helpers shared by the libmlora kernels (sm_103a).
+//
+// Inline PTX for the Blackwell data-movement primitives the kernels are built on:
+// mbarriers with transaction counts, 1-D bulk copies (cp.async.bulk, the TMA engine's
+// untiled form), thread-block-cluster barriers and distributed shared memory.
+// Every wait here is bounded: it gives up after a time limit and reports it.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "launch.h"
+#include "mlora.h"
+
+namespace mlora {
+
+// ---- element types --------------------------------------------------------------------------
+
+template <int DT>
+struct Elem;
+template <>
+struct Elem<MLORA_BF16> {
+  static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+  static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+  static __device__ __forceinline__ uint16_t from_float(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+  }
+};
+template <>
+struct Elem<MLORA_FP16> {
+  static __device__ __forceinline__ float lo(uint32_t w) { return __half2float(__ushort_as_half((uint16_t)w)); }
+  static __device__ __forceinline__ float hi(uint32_t w) {
+    return __half2float(__ushort_as_half((uint16_t)(w >> 16)));
+  }
+  static __device__ __forceinline__ uint16_t from_float(float f) { return __half_as_ushort(__float2half_rn(f)); }
+};
+
+// 8 packed 16-bit elements -> 8 floats
+template <int DT>
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
+  f[0] = Elem<DT>::lo(u.x); f[1] = Elem<DT>::hi(u.x);
+  f[2] = Elem<DT>::lo(u.y); f[3] = Elem<DT>::hi(u.y);
+  f[4] = Elem<DT>::lo(u.z); f[5] = Elem<DT>::hi(u.z);
+  f[6] = Elem<DT>::lo(u.w); f[7] = Elem<DT>::hi(u.w);
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 u;
+  u.x = (uint32_t)Elem<DT>::from_float(f[0]) | ((uint32_t)Elem<DT>::from_float(f[1]) << 16);
+  u.y = (uint32_t)Elem<DT>::from_float(f[2]) | ((uint32_t)Elem<DT>::from_float(f[3]) << 16);
+  u.z = (uint32_t)Elem<DT>::from_float(f[4]) | ((uint32_t)Elem<DT>::from_float(f[5]) << 16);
+  u.w = (uint32_t)Elem<DT>::from_float(f[6]) | ((uint32_t)Elem<DT>::from_float(f[7]) << 16);
+  return u;
+}
+
+// ---- addresses ------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier -------------------------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make the initialised barriers visible to the async proxy and to the cluster.
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase with the given parity to complete, for at most `limit_ns` nanoseconds.
+// Returns false on timeout (the caller reports MLORA_STATUS_TIMEOUT and stops using the stage).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ---- bulk copies (TMA, untiled) ---------------------------------------------------------------
+
+// Copy `bytes` (multiple of 16, both addresses 16-byte aligned) from global to this CTA's
+// shared memory; completion is signalled to `bar` as a transaction count.
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Same, with an L2 eviction-priority hint for data read exactly once (adapter weights).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void bulk_g2s_hint(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_u32(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// ---- clusters and distributed shared memory ------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared-memory address of the same variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(local)), "r"(rank));
+  return out;
+}
+
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// ---- status ---------------------------------------------------------------------------------
+
+__device__ __forceinline__ void report(int32_t *status, int32_t bits) {
+  if (status && bits) atomicOr(status, bits);
+}
+
+}  // namespace mlora

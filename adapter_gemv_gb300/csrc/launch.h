@@ -1,0 +1,47 @@
+// launch.h -- parameter blocks and launchers shared by the C ABI and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mlora.h"
+
+namespace mlora {
+
+struct PoolDev {
+  int32_t kind, dtype, num_slots, num_layers, r_max, d_in, d_out;
+  const uint16_t *a_t, *b, *pages;
+  int64_t page_elems, num_pages;
+  const int32_t *a_tab, *b_tab, *rank;
+  const float *scale;
+};
+
+enum { MODE_SHRINK = 0, MODE_EXPAND = 1, MODE_FUSED = 2 };
+
+// One projection of a launch.
+struct ProblemDev {
+  PoolDev pool;
+  int32_t layer;
+  const uint16_t *x;
+  int64_t ldx;
+  uint16_t *y;
+  int64_t ldy;
+  float *v;  // [M][r_max]
+};
+
+struct DecodeParams {
+  ProblemDev prob[MLORA_MAX_GROUP];
+  int32_t nprob;
+  const int32_t *seg_off, *seg_slot;  // SGMV (seg_off != nullptr)
+  int32_t nseg;
+  const int32_t *row_slot;  // BGMV
+  int32_t M;
+  int32_t *status;
+  // chosen by the launcher
+  int32_t rt, tiles, csplit, kb, nb, sk, se, r_alloc;
+};
+
+// CUDA-core path for decode-sized tiles (decode.cu). force_csplit > 0 overrides the split.
+cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stream, int force_csplit = 0);
+
+}  // namespace mlora

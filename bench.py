@@ -1,0 +1,482 @@
+#!/usr/bin/env python3
+"""Bench: gathered multi-LoRA shrink+expand on GB300, one JSON line on rank 0.
+
+Headline workload (one "step"): the LoRA delta of a whole Llama-2-7B decode step at batch 32,
+Distinct adapters (row i -> adapter i), r = 16, bf16: all seven projections (q, k, v, o
+4096->4096; gate, up 4096->11008; down 11008->4096) of all 32 layers, rows grouped into SGMV
+segments once and reused by every op. The step is issued as 128 grouped fused calls (q/k/v,
+o, gate/up, down per layer) through the C ABI and replayed as a CUDA graph.
+
+  value     rows/s with every input resident in HBM (2.8 GB of algorithmic traffic per step,
+            far above the 129 MB L2, so no flush is needed between steps)
+  e2e       the same metric with the step's inputs (x, base y) copied from pinned host memory
+            and the result y copied back inside the timed region
+  roofline  algorithmic bytes of the step's launches / their time, against the measured HBM copy
+            bandwidth (MEASURED_PEAKS.json)
+  cpu_baseline / --impl reference: the fp64 oracle on the host cores, on a bounded sample of the
+            same step (some of its layers), scaled to the whole step
+  configs   roofline fraction of each of the five workloads (small ones timed per call with an
+            L2 flush in between)
+
+Multi-GPU: the op has no exchange step; N ranks run N independent replicas (weak scaling), with
+a barrier and the max over ranks around the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+from workloads import costmodel as C  # noqa: E402
+
+METRIC = "LoRA shrink+expand rows/s and % of HBM/tensor roofline, 7B decode bs32"
+UNIT = "rows/s"
+WORKLOAD = ("Llama-2-7B decode step, bs32, r16, bf16, Distinct (32 adapters): SGMV delta of q,k,v,o,gate,up,down "
+            "x 32 layers (224 ops)")
+FALLBACK_HBM = 6800.0
+
+
+# ---------------------------------------------------------------------------------------------
+# helpers
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms; keep the samples taken between
+    start() and stop()."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.lines, self.proc, self.t0, self.t1 = [], None, None, None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+        deadline = time.time() + 5
+        while not self.lines and time.time() < deadline:
+            time.sleep(0.05)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def start(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+        time.sleep(0.25)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = [l.split(", ") for t, l in self.lines if self.t0 - 0.2 <= t <= self.t1 + 0.2]
+        rows = [r for r in rows if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip().lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "common.cuh", "launch.h"):
+        h.update(open(os.path.join(ROOT, "adapter_gemv_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload_key: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(workload_key)
+    if not e or e.get("kernel") != kernel or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------------------------
+# the headline step
+
+
+def build_step(dev, dist="distinct"):
+    import adapter_gemv_gb300 as m
+    from adapter_gemv_gb300.plan import StepPlan
+    w = W.sgmv_decode_7b(device=dev, dist=dist)
+    # re-home every base y of the step into one flat buffer (one copy in / one copy out for e2e)
+    total = sum(op.y.numel() for op in w.ops)
+    ybuf = torch.empty(total, dtype=w.dtype, device=dev)
+    o = 0
+    for op in w.ops:
+        n = op.y.numel()
+        ybuf[o:o + n].view_as(op.y).copy_(op.y)
+        op.y = ybuf[o:o + n].view(op.y.shape)
+        o += n
+    xs = []
+    for op in w.ops:
+        if all(op.x.data_ptr() != x.data_ptr() for x in xs):
+            xs.append(op.x)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    plan = StepPlan(w.ops, w.batch, status)
+    return w, plan, ybuf, xs, status, m
+
+
+def step_bytes(w):
+    slots = w.batch.row_slot.cpu().numpy()
+    rs = {id(p): p.rank.cpu().numpy() for p in w.pools}
+    total = 0
+    for op in w.ops:
+        r = rs[id(op.pool)]
+        row_ranks = [int(r[s]) for s in slots if s >= 0]
+        distinct = [int(r[s]) for s in np.unique(slots[slots >= 0])]
+        total += C.op_bytes(d_in=op.pool.d_in, d_out=op.pool.d_out, row_ranks=row_ranks, distinct_ranks=distinct,
+                            v_roundtrip=False)
+    return total
+
+
+def time_graph(graph, stream, steps, sampler=None):
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    start.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    end.record(stream)
+    end.synchronize()
+    if sampler:
+        sampler.stop()
+    return start.elapsed_time(end) / 1e3  # seconds
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn(stream)  # warm: sets kernel attributes outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn(stream)
+    torch.cuda.synchronize()
+    return g
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle on a bounded sample of the step
+
+
+def _oracle_layer_inputs(w, layer):
+    import oracle
+    bits = lambda t: t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    out = []
+    for op in w.ops:
+        if op.layer != layer:
+            continue
+        p = op.pool
+        opool = oracle.Pool(dtype=oracle.DTYPE_BF16, num_slots=p.num_slots, num_layers=1, r_max=p.r_max,
+                            d_in=p.d_in, d_out=p.d_out, rank=p.rank.cpu().numpy(), scale=p.scale.cpu().numpy(),
+                            a_t=bits(p.a_t[:, layer:layer + 1]), b=bits(p.b[:, layer:layer + 1]))
+        out.append((opool, bits(op.x), bits(op.y)))
+    return out
+
+
+def oracle_sample(w, budget_s: float):
+    import oracle
+    off = w.batch.seg_offsets.cpu().numpy()
+    ss = w.batch.seg_slot.cpu().numpy()
+    spent, layers = 0.0, 0
+    for layer in range(32):
+        inputs = _oracle_layer_inputs(w, layer)
+        t0 = time.perf_counter()
+        for opool, x, y in inputs:
+            oracle.sgmv(opool, 0, x, y, off, ss)
+        spent += time.perf_counter() - t0
+        layers += 1
+        if spent >= budget_s:
+            break
+    per_step = spent / layers * 32
+    return per_step, layers
+
+
+# ---------------------------------------------------------------------------------------------
+# per-workload roofline fractions
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def time_calls(fn, stream, iters, flush):
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    with torch.cuda.stream(stream):
+        for k in range(iters):
+            flush_l2(flush)
+            evs[k][0].record(stream)
+            fn(stream)
+            evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) / 1e3 for a, b in evs)
+
+
+def config_fractions(dev, stream, peak, iters=30):
+    import adapter_gemv_gb300 as m
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > 129 MB L2
+    res = {}
+
+    def op_bytes_of(op, batch, v_roundtrip=False):
+        slots = batch.row_slot.cpu().numpy()
+        r = op.pool.rank.cpu().numpy()
+        return C.op_bytes(d_in=op.pool.d_in, d_out=op.pool.d_out, row_ranks=[int(r[s]) for s in slots if s >= 0],
+                          distinct_ranks=[int(r[s]) for s in np.unique(slots[slots >= 0])], v_roundtrip=v_roundtrip)
+
+    def single(name, w, form):
+        op = w.ops[0]
+        h = m.make_pool(op.pool)
+        v = torch.empty((w.batch.M, op.pool.r_max), dtype=torch.float32, device=dev)
+        b = w.batch
+        if form == "sgmv":
+            fused = lambda s: m.lora_sgmv(op.y, op.x, h, b.seg_offsets, b.seg_slot, op.layer, v, stream=s)
+            two = lambda s: (m.lora_sgmv_shrink(v, op.x, h, b.seg_offsets, b.seg_slot, op.layer, stream=s),
+                             m.lora_sgmv_expand(op.y, v, h, b.seg_offsets, b.seg_slot, op.layer, stream=s))
+        else:
+            fused = lambda s: m.lora_bgmv(op.y, op.x, h, b.row_slot, op.layer, v, stream=s)
+            two = lambda s: (m.lora_bgmv_shrink(v, op.x, h, b.row_slot, op.layer, stream=s),
+                             m.lora_bgmv_expand(op.y, v, h, b.row_slot, op.layer, stream=s))
+        out = {}
+        for label, fn, vr in (("fused", fused, False), ("two_launch", two, True)):
+            t = time_calls(fn, stream, iters, flush)
+            by = op_bytes_of(op, b, vr)
+            out[label] = {"us": round(t * 1e6, 2), "bytes": by, "gbs": round(by / t / 1e9, 1),
+                          "frac": round(by / t / 1e9 / peak, 4)}
+        res[name] = out
+
+    single("1_tiny_sgmv_fp16", W.tiny_sgmv(device=dev), "sgmv")
+    single("2_bgmv_q_proj_distinct", W.bgmv_decode_q(device=dev), "bgmv")
+    for dist in ("distinct", "uniform", "skewed", "identical"):
+        w, plan, *_ = build_step(dev, dist)
+        g = capture(plan, stream)
+        t = time_graph(g, stream, 20) / 20
+        by = step_bytes(w)
+        res[f"3_decode_7b_{dist}"] = {"us_per_step": round(t * 1e6, 1), "bytes": by, "gbs": round(by / t / 1e9, 1),
+                                      "frac": round(by / t / 1e9 / peak, 4), "launches": plan.launches}
+        del w, plan, g
+        torch.cuda.empty_cache()
+    w = W.sgmv_prefill_13b(device=dev)
+    tot_t, tot_b = 0.0, 0
+    for op in w.ops:
+        h = m.make_pool(op.pool)
+        v = torch.empty((w.batch.M, op.pool.r_max), dtype=torch.float32, device=dev)
+        fn = lambda s, op=op, h=h, v=v: m.lora_sgmv(op.y, op.x, h, w.batch.seg_offsets, w.batch.seg_slot, 0, v,
+                                                     stream=s)
+        tot_t += time_calls(fn, stream, 5, flush)
+        tot_b += op_bytes_of(op, w.batch)
+    res["4_prefill_13b"] = {"us_7_ops": round(tot_t * 1e6, 1), "bytes": tot_b, "gbs": round(tot_b / tot_t / 1e9, 1),
+                            "frac": round(tot_b / tot_t / 1e9 / peak, 4), "rows": w.batch.M}
+    del w
+    torch.cuda.empty_cache()
+    single("5_paged_hetero_70b", W.paged_decode_70b(device=dev), "bgmv")
+    return res
+
+
+# ---------------------------------------------------------------------------------------------
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    hbm, peak_kind = peaks()
+
+    w, plan, ybuf, xs, status, m = build_step(dev, "distinct")
+    rows = w.batch.M
+    bytes_step = step_bytes(w)
+    g = capture(plan, stream)
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {status.item()} during warm-up")
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    barrier()
+    secs = time_graph(g, stream, args.steps, sampler)
+    barrier()
+    if ws > 1:
+        t = torch.tensor([secs], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        secs = float(t.item())
+    ms = secs / args.steps * 1e3
+    value = ws * rows * args.steps / secs
+
+    # e2e: pinned host inputs -> device, the step, result back to the host, every step
+    host_y = torch.empty(ybuf.shape, dtype=ybuf.dtype, pin_memory=True)
+    host_y.copy_(ybuf)
+    host_out = torch.empty_like(host_y, pin_memory=True)
+    host_x = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x) for x in xs]
+    e2e_steps = max(3, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        def e2e_once():
+            ybuf.copy_(host_y, non_blocking=True)
+            for hx, x in zip(host_x, xs):
+                x.copy_(hx, non_blocking=True)
+            g.replay()
+            host_out.copy_(ybuf, non_blocking=True)
+        for _ in range(2):
+            e2e_once()
+        barrier()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_once()
+        ev1.record(stream)
+        ev1.synchronize()
+    e2e_secs = ev0.elapsed_time(ev1) / 1e3
+    if ws > 1:
+        t = torch.tensor([e2e_secs], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_secs = float(t.item())
+    h2d = ybuf.numel() * ybuf.element_size() + sum(x.numel() * x.element_size() for x in xs)
+    d2h = ybuf.numel() * ybuf.element_size()
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    achieved = bytes_step / (secs / args.steps) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": rows * ws, "rows_per_step_per_gpu": rows, "rank": 16,
+                   "ops_per_step": len(w.ops), "launch": f"CUDA graph of {plan.launches} grouped fused calls",
+                   "l2": "inputs larger than L2 (2.8 GB of adapter weights and activations per step)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                     "kernel": "decode_kernel<bf16, FUSED> (every launch of the step)",
+                     "algorithmic_bytes_per_launch": bytes_step // plan.launches,
+                     "traffic": ncu_traffic("decode_kernel_fused", "decode7b_distinct")},
+        "e2e": {"value": round(rows * e2e_steps / e2e_secs * ws, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_secs / e2e_steps * 1e3, 4),
+                "api": "lora_sgmv_grouped via the Python binding, replayed as a CUDA graph; pinned host buffers"},
+        "gpu_launches": plan.launches * args.steps,
+        "clocks": sampler.summary() if sampler else None,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        per_step, layers = oracle_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(rows / per_step, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"fp64 oracle on {layers} of 32 layers (all 7 ops each) of the same step, "
+                                          f"single thread, scaled x{32 / layers:.2f} to the step"}
+    del g, plan, w
+    torch.cuda.empty_cache()
+    if not args.no_configs:
+        line["configs"] = config_fractions(dev, stream, hbm)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as the reference arm: host cores, bounded sample per step, same metric."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = W.sgmv_decode_7b(device="cpu", dist="distinct", num_layers=2)  # per-layer work equals the full step's
+    import oracle
+    off, ss = w.batch.seg_offsets.numpy(), w.batch.seg_slot.numpy()
+    per_layer = {layer: _oracle_layer_inputs(w, layer) for layer in range(2)}
+    def one(layer):
+        t0 = time.perf_counter()
+        for opool, x, y in per_layer[layer]:
+            oracle.sgmv(opool, 0, x, y, off, ss)
+        return time.perf_counter() - t0
+    for k in range(args.warmup):
+        one(k % 2)
+    times = [one(k % 2) for k in range(args.steps)]
+    per_step = sum(times) / len(times) * 32
+    value = w.batch.M / per_step
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "each step: the fp64 oracle on one layer (7 ops) of the step, x32"},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+"""GPU edge cases against the oracle: random segment layouts (empty segments, repeated slots,
+-1 segments), ragged sizes, ranks 1..128 (the maximum), stacked and paged pools, both dtypes,
+guard regions around every output, the device status contract, determinism, and the
+equivalences between the call forms."""
+import numpy as np
+import pytest
+import torch
+
+import adapter_gemv_gb300 as m
+import oracle
+import workloads as W
+from gpu_util import assert_close, bits, check_op, new_v, odt, oracle_pool
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import os
+    if not os.path.exists(m.LIB_PATH):
+        from adapter_gemv_gb300 import build
+        build.build()
+    return torch.device("cuda:0")
+
+
+def make_case(dev, seed, *, dtype, paged, r_max, d_in, d_out, M, num_slots=5, num_layers=2, max_seg=9):
+    rng = np.random.default_rng(seed)
+    g = W.generator(seed, dev)
+    ranks = rng.integers(1, r_max + 1, num_slots).astype(np.int32)
+    ranks[0] = r_max
+    ranks[-1] = 1
+    if paged:
+        pool = W.paged_pool(num_slots=num_slots, num_layers=num_layers, r_max=r_max, d_in=d_in, d_out=d_out,
+                            dtype=dtype, gen=g, device=dev, rng=rng, ranks=ranks,
+                            page_elems=max(d_in, d_out) + 8 * int(rng.integers(0, 3)))
+    else:
+        pool = W.stacked_pool(num_slots=num_slots, num_layers=num_layers, r_max=r_max, d_in=d_in, d_out=d_out,
+                              dtype=dtype, gen=g, device=dev, ranks=ranks)
+    # segments: random lengths (some empty), random slots with -1 and repeats, summing to M
+    nseg = int(rng.integers(1, max_seg + 1))
+    cuts = np.sort(rng.integers(0, M + 1, nseg - 1)) if nseg > 1 else np.array([], int)
+    off = np.r_[0, cuts, M].astype(np.int32)
+    seg_slot = rng.integers(-1, num_slots, nseg).astype(np.int32)
+    lens = np.diff(off)
+    batch = W.Batch(M, torch.from_numpy(np.repeat(seg_slot, lens).astype(np.int32)), torch.from_numpy(off),
+                    torch.from_numpy(seg_slot)).to(dev)
+    x = W.normal((M, d_in), 1.0, dtype, g, dev)
+    y = W.uniform((M, d_out), -1, 1, dtype, g, dev)
+    layer = int(rng.integers(0, num_layers))
+    return W.Op("fuzz", pool, layer, x, y), batch
+
+
+class Guarded:
+    """y and v inside larger buffers: guard rows before/after and guard columns past d_out."""
+
+    def __init__(self, y: torch.Tensor, r_max: int, pad_cols=8):
+        M, d = y.shape
+        self.ybuf = torch.empty((M + 2, d + pad_cols), dtype=y.dtype, device=y.device)
+        self.ybuf.view(torch.int16).fill_(0x5A5A)
+        self.y = self.ybuf[1:M + 1, :d]
+        self.y.copy_(y)
+        self.vbuf = torch.full(((M + 2) * r_max,), 1234.5, dtype=torch.float32, device=y.device)
+        self.v = self.vbuf[r_max:r_max + M * r_max].view(M, r_max)
+        self.M, self.d, self.r = M, d, r_max
+
+    def check(self, v_written: bool):
+        yb = bits(self.ybuf)
+        assert np.all(yb[0] == 0x5A5A) and np.all(yb[-1] == 0x5A5A), "y guard rows written"
+        assert np.all(yb[:, self.d:] == 0x5A5A), "y guard columns written"
+        vb = self.vbuf.cpu().numpy()
+        assert np.all(vb[:self.r] == 1234.5) and np.all(vb[self.r + self.M * self.r:] == 1234.5), "v guards written"
+
+
+SHAPES = [
+    # dtype, paged, r_max, d_in, d_out, M
+    (torch.bfloat16, False, 16, 264, 40, 33),
+    (torch.float16, False, 8, 24, 520, 7),
+    (torch.bfloat16, True, 64, 1032, 264, 130),
+    (torch.float16, True, 1, 8, 8, 5),
+    (torch.bfloat16, False, 128, 4104, 2056, 21),
+    (torch.bfloat16, True, 128, 520, 4104, 12),
+    (torch.float16, False, 32, 16384, 64, 3),
+    (torch.bfloat16, False, 64, 96, 16384, 9),
+    (torch.bfloat16, False, 16, 4096, 4096, 1),
+    (torch.bfloat16, False, 16, 4096, 4096, 0),
+]
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"{'bf16' if s[0] == torch.bfloat16 else 'fp16'}-"
+                         f"{'paged' if s[1] else 'stacked'}-r{s[2]}-{s[3]}x{s[4]}-M{s[5]}")
+@pytest.mark.parametrize("form", ["sgmv", "bgmv"])
+def test_fuzz_two_phase_and_fused(dev, shape, seed, form):
+    dtype, paged, r_max, d_in, d_out, M = shape
+    op, batch = make_case(dev, 100 + seed, dtype=dtype, paged=paged, r_max=r_max, d_in=d_in, d_out=d_out, M=M)
+    pool = m.make_pool(op.pool)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    # two launches, with guard regions
+    g2 = Guarded(op.y, r_max)
+    if form == "sgmv":
+        m.lora_sgmv_shrink(g2.v, op.x, pool, batch.seg_offsets, batch.seg_slot, op.layer, st)
+        m.lora_sgmv_expand(g2.y, g2.v, pool, batch.seg_offsets, batch.seg_slot, op.layer, st)
+    else:
+        m.lora_bgmv_shrink(g2.v, op.x, pool, batch.row_slot, op.layer, st)
+        m.lora_bgmv_expand(g2.y, g2.v, pool, batch.row_slot, op.layer, st)
+    # fused, with guard regions
+    g1 = Guarded(op.y, r_max)
+    if form == "sgmv":
+        m.lora_sgmv(g1.y, op.x, pool, batch.seg_offsets, batch.seg_slot, op.layer, g1.v, st)
+    else:
+        m.lora_bgmv(g1.y, op.x, pool, batch.row_slot, op.layer, g1.v, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    g2.check(True)
+    g1.check(False)
+    check_op(op, batch, form, g2.y, g2.v, what="two-phase")
+    check_op(op, batch, form, g1.y, what="fused")
+
+
+def test_status_contract_matches_oracle(dev):
+    """Bad offsets / slots / ranks / pages: same status bits as the oracle, affected rows
+    untouched bit for bit, all other rows correct."""
+    dt = torch.bfloat16
+    op, batch = make_case(dev, 7, dtype=dt, paged=True, r_max=16, d_in=64, d_out=48, M=12, num_slots=4)
+    pool = op.pool
+    op_pool = oracle_pool(pool)
+
+    def both(form, meta, rank=None, a_tab=None, b_tab=None):
+        rk = pool.rank if rank is None else rank
+        at = pool.a_page_table if a_tab is None else a_tab
+        bt = pool.b_page_table if b_tab is None else b_tab
+        p2 = W.Pool(dt, pool.num_slots, pool.num_layers, pool.r_max, pool.d_in, pool.d_out, rk, pool.scale,
+                    pages=pool.pages, a_page_table=at, b_page_table=bt)
+        h = m.make_pool(p2)
+        y = op.y.clone()
+        v = new_v(12, 16, dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        if form == "sgmv":
+            off, ss = meta
+            m.lora_sgmv(y, op.x, h, off.to(dev), ss.to(dev), op.layer, v, st)
+        else:
+            m.lora_bgmv(y, op.x, h, meta.to(dev), op.layer, v, st)
+        torch.cuda.synchronize()
+        opool = oracle.Pool(dtype=odt(dt), num_slots=p2.num_slots, num_layers=p2.num_layers, r_max=16, d_in=64,
+                            d_out=48, rank=rk.cpu().numpy(), scale=pool.scale.cpu().numpy(),
+                            pages=op_pool.pages, a_page_table=at.cpu().numpy(), b_page_table=bt.cpu().numpy())
+        if form == "sgmv":
+            yo, _, _, so = oracle.sgmv(opool, op.layer, bits(op.x), bits(op.y), meta[0].numpy(), meta[1].numpy())
+        else:
+            yo, _, _, so = oracle.bgmv(opool, op.layer, bits(op.x), bits(op.y), meta.numpy())
+        return bits(y), yo, int(st.item()), so
+
+    t = lambda a: torch.tensor(a, dtype=torch.int32)
+    for off in ([1, 5, 12], [0, 7, 5, 12], [0, 6, 13]):
+        g, o, sg, so = both("sgmv", (t(off), t([0] * (len(off) - 1))))
+        assert sg == so == m.STATUS_BAD_OFFSETS and np.array_equal(g, bits(op.y))
+    slots = t([0, 9, -1, 1, -3, 2, 3, 0, 1, 2, 3, -1])
+    g, o, sg, so = both("bgmv", slots)
+    assert sg == so == m.STATUS_BAD_SLOT
+    for i in (1, 2, 4, 11):
+        assert np.array_equal(g[i], bits(op.y)[i])
+    ok_rows = [i for i in range(12) if i not in (1, 2, 4, 11)]
+    assert_close(oracle.decode(g[ok_rows], odt(dt)), oracle.decode(o[ok_rows], odt(dt)), "status bgmv")
+    rk = pool.rank.clone()
+    rk[1] = 0
+    rk[2] = 17
+    g, o, sg, so = both("bgmv", t([0, 1, 2, 3] * 3), rank=rk)
+    assert sg == so == m.STATUS_BAD_RANK
+    assert np.array_equal(g[1::4], bits(op.y)[1::4]) and np.array_equal(g[2::4], bits(op.y)[2::4])
+    at = pool.a_page_table.clone()
+    at[3, op.layer, 0] = pool.pages.shape[0]
+    g, o, sg, so = both("bgmv", t([0, 1, 2, 3] * 3), a_tab=at)
+    assert sg == so == m.STATUS_BAD_PAGE and np.array_equal(g[3::4], bits(op.y)[3::4])
+    assert_close(oracle.decode(g[0::4], odt(dt)), oracle.decode(o[0::4], odt(dt)), "bad page, other rows")
+
+
+def test_minus_one_rows_keep_nan_payloads(dev):
+    op, batch = make_case(dev, 11, dtype=torch.bfloat16, paged=False, r_max=8, d_in=64, d_out=64, M=6)
+    y = op.y.clone()
+    y[1].view(torch.int16).fill_(0x7F85)  # NaN with a payload
+    y[3].view(torch.int16).fill_(-0x8000)  # -0.0
+    slots = torch.tensor([0, -1, 1, -1, 2, 0], dtype=torch.int32, device=dev)
+    yb = bits(y)
+    h = m.make_pool(op.pool)
+    m.lora_bgmv(y, op.x, h, slots, op.layer, new_v(6, 8, dev))
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(y)[[1, 3]], yb[[1, 3]])
+
+
+def test_deterministic_and_forms_agree_bitwise(dev):
+    """Same inputs twice: identical bits. BGMV on rows grouped like an SGMV batch, SGMV, and
+    a grouped call of identical problems: identical bits."""
+    w = W.sgmv_decode_7b(device=dev, dist="uniform", num_layers=1)
+    op = w.ops[0]
+    h = m.make_pool(op.pool)
+    outs = []
+    for _ in range(2):
+        y = op.y.clone()
+        m.lora_sgmv(y, op.x, h, w.batch.seg_offsets, w.batch.seg_slot, 0, new_v(32, 16, dev))
+        outs.append(bits(y))
+    yb = op.y.clone()
+    m.lora_bgmv(yb, op.x, h, w.batch.row_slot, 0, new_v(32, 16, dev))
+    yg = [op.y.clone() for _ in range(3)]
+    m.lora_sgmv_grouped([(yg[q], op.x, h, 0, new_v(32, 16, dev)) for q in range(3)], w.batch.seg_offsets,
+                        w.batch.seg_slot)
+    torch.cuda.synchronize()
+    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[0], bits(yb))
+    for q in range(3):
+        assert np.array_equal(outs[0], bits(yg[q]))
+    # two-phase form: same v twice
+    v1, v2 = new_v(32, 16, dev), new_v(32, 16, dev)
+    m.lora_sgmv_shrink(v1, op.x, h, w.batch.seg_offsets, w.batch.seg_slot, 0)
+    m.lora_sgmv_shrink(v2, op.x, h, w.batch.seg_offsets, w.batch.seg_slot, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(v1, v2)
+
+
+def test_host_errors_launch_nothing(dev):
+    op, batch = make_case(dev, 3, dtype=torch.bfloat16, paged=False, r_max=8, d_in=64, d_out=64, M=4)
+    before = m.launch_count()
+    with pytest.raises(m.MloraError) as e:
+        m.lora_sgmv(op.y, op.x, op.pool, batch.seg_offsets, batch.seg_slot, 5, new_v(4, 8, dev))
+    assert e.value.code == m.ERR_SHAPE
+    with pytest.raises(m.MloraError) as e:
+        m.lora_sgmv(op.y[:, 1:], op.x, op.pool, batch.seg_offsets, batch.seg_slot, 0, new_v(4, 8, dev))
+    assert e.value.code in (m.ERR_ALIGN, m.ERR_SHAPE)
+    assert m.launch_count() == before
