@@ -84,6 +84,8 @@ def lib():
                 L.lora_error_string.restype = ctypes.c_char_p
                 L.lora_abi_version.restype = ctypes.c_int
                 L.lora_launch_count.restype = ctypes.c_int64
+                L.lora_set_programmatic_launch.argtypes = [ctypes.c_int]
+                L.lora_set_programmatic_launch.restype = ctypes.c_int
                 _lib = L
     return _lib
 
@@ -236,6 +238,12 @@ def lora_sgmv_grouped(problems, seg_offsets, seg_slot, status=None, stream=None)
 
 def launch_count() -> int:
     return int(lib().lora_launch_count())
+
+
+def lora_set_programmatic_launch(enable: bool) -> bool:
+    """Process-wide switch for programmatic dependent launch (see include/mlora.h); returns the
+    previous setting."""
+    return bool(lib().lora_set_programmatic_launch(1 if enable else 0))
 
 
 def abi_version() -> int:

@@ -17,6 +17,7 @@ namespace {
 
 thread_local char g_cuda_err[256] = "no CUDA error recorded";
 std::atomic<int64_t> g_launches{0};
+std::atomic<int> g_pdl{0};
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -72,21 +73,25 @@ mlora::PoolDev to_dev(const mlora_pool *p) {
   return d;
 }
 
-int check_x(const void *x, int64_t ldx, const mlora_pool *p) {
+// With zero rows the activation, output and v pointers may be NULL (empty arrays).
+int check_x(const void *x, int64_t ldx, const mlora_pool *p, int32_t rows) {
+  if (rows == 0) return MLORA_OK;
   if (!x) return MLORA_ERR_NULL;
   if (ldx < p->d_in) return MLORA_ERR_SHAPE;
   if (!aligned(x, 16) || ldx % 8) return MLORA_ERR_ALIGN;
   return MLORA_OK;
 }
 
-int check_y(const void *y, int64_t ldy, const mlora_pool *p) {
+int check_y(const void *y, int64_t ldy, const mlora_pool *p, int32_t rows) {
+  if (rows == 0) return MLORA_OK;
   if (!y) return MLORA_ERR_NULL;
   if (ldy < p->d_out) return MLORA_ERR_SHAPE;
   if (!aligned(y, 16) || ldy % 8) return MLORA_ERR_ALIGN;
   return MLORA_OK;
 }
 
-int check_v(const float *v) {
+int check_v(const float *v, int32_t rows) {
+  if (rows == 0) return MLORA_OK;
   if (!v) return MLORA_ERR_NULL;
   if (!aligned(v, 4)) return MLORA_ERR_ALIGN;
   return MLORA_OK;
@@ -125,7 +130,7 @@ mlora::DecodeParams base_params(const int32_t *off, const int32_t *seg_slot, int
 }
 
 int run(int mode, int dtype, const mlora::DecodeParams &d, void *stream) {
-  const cudaError_t e = mlora::launch_decode(mode, dtype, d, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = mlora::launch_decode(mode, dtype, d, static_cast<cudaStream_t>(stream), g_pdl.load() != 0);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return MLORA_OK;
@@ -152,8 +157,8 @@ int lora_sgmv_shrink(float *v, const void *x, int64_t ldx, const mlora_pool *poo
                      const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t layer,
                      int32_t *dev_status, void *stream) {
   TRY(check_pool(pool, layer, true, false));
-  TRY(check_v(v));
-  TRY(check_x(x, ldx, pool));
+  TRY(check_v(v, num_rows));
+  TRY(check_x(x, ldx, pool, num_rows));
   TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
   mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
@@ -166,8 +171,8 @@ int lora_sgmv_expand(void *y, int64_t ldy, const float *v, const mlora_pool *poo
                      const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t layer,
                      int32_t *dev_status, void *stream) {
   TRY(check_pool(pool, layer, false, true));
-  TRY(check_v(v));
-  TRY(check_y(y, ldy, pool));
+  TRY(check_v(v, num_rows));
+  TRY(check_y(y, ldy, pool, num_rows));
   TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
   mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
@@ -179,8 +184,8 @@ int lora_sgmv_expand(void *y, int64_t ldy, const float *v, const mlora_pool *poo
 int lora_bgmv_shrink(float *v, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
                      int32_t num_rows, int32_t layer, int32_t *dev_status, void *stream) {
   TRY(check_pool(pool, layer, true, false));
-  TRY(check_v(v));
-  TRY(check_x(x, ldx, pool));
+  TRY(check_v(v, num_rows));
+  TRY(check_x(x, ldx, pool, num_rows));
   TRY(check_rows_bgmv(row_slot, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
   mlora::DecodeParams d = base_params(nullptr, nullptr, 0, row_slot, num_rows, dev_status);
@@ -192,8 +197,8 @@ int lora_bgmv_shrink(float *v, const void *x, int64_t ldx, const mlora_pool *poo
 int lora_bgmv_expand(void *y, int64_t ldy, const float *v, const mlora_pool *pool, const int32_t *row_slot,
                      int32_t num_rows, int32_t layer, int32_t *dev_status, void *stream) {
   TRY(check_pool(pool, layer, false, true));
-  TRY(check_v(v));
-  TRY(check_y(y, ldy, pool));
+  TRY(check_v(v, num_rows));
+  TRY(check_y(y, ldy, pool, num_rows));
   TRY(check_rows_bgmv(row_slot, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
   mlora::DecodeParams d = base_params(nullptr, nullptr, 0, row_slot, num_rows, dev_status);
@@ -206,9 +211,9 @@ int lora_sgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool
               const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t layer, float *v_scratch,
               int32_t *dev_status, void *stream) {
   TRY(check_pool(pool, layer, true, true));
-  TRY(check_v(v_scratch));
-  TRY(check_x(x, ldx, pool));
-  TRY(check_y(y, ldy, pool));
+  TRY(check_v(v_scratch, num_rows));
+  TRY(check_x(x, ldx, pool, num_rows));
+  TRY(check_y(y, ldy, pool, num_rows));
   TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
   mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
@@ -220,9 +225,9 @@ int lora_sgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool
 int lora_bgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
               int32_t num_rows, int32_t layer, float *v_scratch, int32_t *dev_status, void *stream) {
   TRY(check_pool(pool, layer, true, true));
-  TRY(check_v(v_scratch));
-  TRY(check_x(x, ldx, pool));
-  TRY(check_y(y, ldy, pool));
+  TRY(check_v(v_scratch, num_rows));
+  TRY(check_x(x, ldx, pool, num_rows));
+  TRY(check_y(y, ldy, pool, num_rows));
   TRY(check_rows_bgmv(row_slot, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
   mlora::DecodeParams d = base_params(nullptr, nullptr, 0, row_slot, num_rows, dev_status);
@@ -242,9 +247,9 @@ int lora_sgmv_grouped(const mlora_problem *problems, int32_t num_problems, const
     const mlora_problem &pb = problems[q];
     TRY(check_pool(pb.pool, pb.layer, true, true));
     if (pb.pool->dtype != problems[0].pool->dtype) return MLORA_ERR_DTYPE;
-    TRY(check_v(pb.v_scratch));
-    TRY(check_x(pb.x, pb.ldx, pb.pool));
-    TRY(check_y(pb.y, pb.ldy, pb.pool));
+    TRY(check_v(pb.v_scratch, num_rows));
+    TRY(check_x(pb.x, pb.ldx, pb.pool, num_rows));
+    TRY(check_y(pb.y, pb.ldy, pb.pool, num_rows));
     d.prob[q] = problem(pb.pool, pb.layer, pb.x, pb.ldx, pb.y, pb.ldy, pb.v_scratch);
   }
   d.nprob = num_problems;
@@ -266,6 +271,8 @@ const char *lora_error_string(int code) {
 }
 
 int lora_abi_version(void) { return MLORA_ABI_VERSION; }
+
+int lora_set_programmatic_launch(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
 int64_t lora_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

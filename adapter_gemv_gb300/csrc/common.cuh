@@ -109,6 +109,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
   }
 }
 
+// Same wait with cluster-scope acquire: for barriers completed by peers' st.async pushes.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ---- programmatic dependent launch -------------------------------------------------------------
+
+// Allow the next kernel in the stream to be scheduled now (it still waits for this grid to
+// finish before griddepcontrol.wait returns in it).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Wait until every grid this one depends on has completed and its memory is visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- bulk copies (TMA, untiled) ---------------------------------------------------------------
 
 // Copy `bytes` (multiple of 16, both addresses 16-byte aligned) from global to this CTA's
@@ -143,6 +175,22 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
+}
+
+// Split cluster barrier: arrive (relaxed; the mbarrier-init fence already released the barriers)
+// and, later, wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Store one float into a peer CTA's shared memory; the store completes as 4 transaction bytes
+// on the peer's mbarrier (both addresses from mapa).
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote_addr), "f"(v),
+               "r"(remote_bar)
+               : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {

@@ -41,7 +41,15 @@ struct DecodeParams {
   int32_t rt, tiles, csplit, kb, nb, sk, se, r_alloc;
 };
 
-// CUDA-core path for decode-sized tiles (decode.cu). force_csplit > 0 overrides the split.
-cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stream, int force_csplit = 0);
+// CUDA-core path for decode-sized tiles (decode_launch.cu chooses the split and the stages;
+// decode_{shrink,expand,fused}.cu hold the kernels). force_csplit > 0 overrides the split.
+cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stream, bool pdl, int force_csplit = 0);
+
+cudaError_t launch_decode_shrink(int dtype, const DecodeParams &p, unsigned grid, size_t smem, int cluster, bool pdl,
+                                 cudaStream_t stream);
+cudaError_t launch_decode_expand(int dtype, const DecodeParams &p, unsigned grid, size_t smem, int cluster, bool pdl,
+                                 cudaStream_t stream);
+cudaError_t launch_decode_fused(int dtype, const DecodeParams &p, unsigned grid, size_t smem, int cluster, bool pdl,
+                                cudaStream_t stream);
 
 }  // namespace mlora

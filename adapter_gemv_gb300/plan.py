@@ -12,12 +12,17 @@ from typing import List, Sequence
 
 import torch
 
-from . import MLORA_MAX_GROUP, Group, make_pool
+from . import MLORA_MAX_GROUP, Group, lora_set_programmatic_launch, make_pool
 
 
 class StepPlan:
-    def __init__(self, ops: Sequence, batch, status=None):
-        """ops: objects with .pool .layer .x .y (as workloads.Op); batch: .M .seg_offsets .seg_slot."""
+    def __init__(self, ops: Sequence, batch, status=None, programmatic: bool = True):
+        """ops: objects with .pool .layer .x .y (as workloads.Op); batch: .M .seg_offsets .seg_slot.
+        programmatic: launch every call but the first with programmatic dependent launch. Safe
+        because the kernel before each of those calls is this library's previous call, which
+        writes none of the inputs a call reads before its wait (metadata, pool). The first call
+        keeps an ordinary dependency on whatever ran before the step."""
+        self.programmatic = programmatic
         self.handles = {}
         groups: List[List] = []
         for op in ops:
@@ -43,8 +48,14 @@ class StepPlan:
         self.groups = groups
 
     def __call__(self, stream=None):
-        for c in self.calls:
-            c(stream)
+        prev = lora_set_programmatic_launch(False)
+        try:
+            for q, c in enumerate(self.calls):
+                if q == 1:
+                    lora_set_programmatic_launch(self.programmatic)
+                c(stream)
+        finally:
+            lora_set_programmatic_launch(prev)
 
     @property
     def launches(self) -> int:

@@ -185,10 +185,11 @@ def time_graph(graph, stream, steps, sampler=None):
     torch.cuda.synchronize()
     if sampler:
         sampler.start()
-    start.record(stream)
-    for _ in range(steps):
-        graph.replay()
-    end.record(stream)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        start.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        end.record(stream)
     end.synchronize()
     if sampler:
         sampler.stop()
@@ -252,15 +253,24 @@ def flush_l2(buf):
 
 
 def time_calls(fn, stream, iters, flush):
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
-    with torch.cuda.stream(stream):
-        for k in range(iters):
+    """Device time of one call with a cold L2: replay a graph of `iters` x [flush, call] and one of
+    `iters` x [flush], both without host gaps, and take the difference per call."""
+    def body_both(s):
+        for _ in range(iters):
             flush_l2(flush)
-            evs[k][0].record(stream)
-            fn(stream)
-            evs[k][1].record(stream)
-    torch.cuda.synchronize()
-    return statistics.median(a.elapsed_time(b) / 1e3 for a, b in evs)
+            fn(s)
+
+    def body_flush(s):
+        for _ in range(iters):
+            flush_l2(flush)
+
+    g_both, g_flush = capture(body_both, stream), capture(body_flush, stream)
+    best = []
+    for _ in range(3):
+        tb = time_graph(g_both, stream, 1)
+        tf = time_graph(g_flush, stream, 1)
+        best.append((tb - tf) / iters)
+    return max(min(best), 1e-9)
 
 
 def config_fractions(dev, stream, peak, iters=30):
@@ -340,8 +350,9 @@ def run_ours(args):
     rows = w.batch.M
     bytes_step = step_bytes(w)
     g = capture(plan, stream)
-    for _ in range(args.warmup):
-        g.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {status.item()} during warm-up")

@@ -49,8 +49,9 @@
  *     of adapted rows (other entries unspecified), read by expand.
  *   - Alignment (16-byte rows for bulk copies): x, y, a_t, b, pages 16-byte aligned; ldx,
  *     ldy, d_in, d_out, page_elems multiples of 8 elements; v 4-byte aligned.
- *   - Limits: 1 <= r_max <= MLORA_MAX_RANK; d_in, d_out >= 8; num_rows >= 0 (0 is a no-op);
- *     0 <= layer < num_layers; num_segments >= 0.
+ *   - Limits: 1 <= r_max <= MLORA_MAX_RANK; d_in, d_out >= 8; num_rows >= 0; 0 <= layer <
+ *     num_layers; num_segments >= 0. num_rows == 0 is a no-op that launches nothing; then x,
+ *     y, v and row_slot may be NULL (empty arrays), the pool is still validated.
  *   - Host-detectable errors return a negative MLORA_ERR_* code BEFORE anything is launched
  *     (nothing is written). A failed launch returns MLORA_ERR_CUDA (text: lora_error_string).
  *   - Device-detectable metadata errors never trap: the kernel ORs an MLORA_STATUS_* bit
@@ -183,6 +184,16 @@ MLORA_API int lora_sgmv_grouped(const mlora_problem *problems, int32_t num_probl
 
 /* Static text for a return code; for MLORA_ERR_CUDA it names the last CUDA error this thread saw. */
 MLORA_API const char *lora_error_string(int code);
+
+/* Programmatic dependent launch (off by default). When on, every later call launches its
+ * kernel so that it may start while the previous kernel in the stream is still running: before
+ * waiting for that kernel it reads only its rows' metadata (offsets, slots), the pool descriptor
+ * arrays (rank, scale, page tables) and the adapter weights, and it requests the weights; x, y
+ * and v are touched only after the wait. Turn it on only where the kernel launched just before
+ * each call does not write those inputs -- e.g. a sequence of this library's calls, or calls
+ * whose inputs were written by copies or at least one kernel earlier. Process-wide; returns
+ * the previous setting. (No counterpart on the pages: a launch-latency measure for GB300.) */
+MLORA_API int lora_set_programmatic_launch(int enable);
 
 /* MLORA_ABI_VERSION of the loaded library. */
 MLORA_API int lora_abi_version(void);

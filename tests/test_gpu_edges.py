@@ -189,9 +189,10 @@ def test_minus_one_rows_keep_nan_payloads(dev):
     assert np.array_equal(bits(y)[[1, 3]], yb[[1, 3]])
 
 
-def test_deterministic_and_forms_agree_bitwise(dev):
-    """Same inputs twice: identical bits. BGMV on rows grouped like an SGMV batch, SGMV, and
-    a grouped call of identical problems: identical bits."""
+def test_deterministic_and_forms_agree(dev):
+    """Same call twice: identical bits (fixed summation order, no atomics). BGMV on rows grouped
+    like an SGMV batch, SGMV, and a grouped call all match the oracle; their split of d_in may
+    differ (it follows the tile count), so they agree within tolerance, not bit for bit."""
     w = W.sgmv_decode_7b(device=dev, dist="uniform", num_layers=1)
     op = w.ops[0]
     h = m.make_pool(op.pool)
@@ -199,18 +200,19 @@ def test_deterministic_and_forms_agree_bitwise(dev):
     for _ in range(2):
         y = op.y.clone()
         m.lora_sgmv(y, op.x, h, w.batch.seg_offsets, w.batch.seg_slot, 0, new_v(32, 16, dev))
-        outs.append(bits(y))
+        outs.append(y)
     yb = op.y.clone()
     m.lora_bgmv(yb, op.x, h, w.batch.row_slot, 0, new_v(32, 16, dev))
     yg = [op.y.clone() for _ in range(3)]
     m.lora_sgmv_grouped([(yg[q], op.x, h, 0, new_v(32, 16, dev)) for q in range(3)], w.batch.seg_offsets,
                         w.batch.seg_slot)
     torch.cuda.synchronize()
-    assert np.array_equal(outs[0], outs[1])
-    assert np.array_equal(outs[0], bits(yb))
+    assert np.array_equal(bits(outs[0]), bits(outs[1]))
+    check_op(op, w.batch, "sgmv", outs[0], what="sgmv")
+    check_op(op, w.batch, "bgmv", yb, what="bgmv of the grouped rows")
     for q in range(3):
-        assert np.array_equal(outs[0], bits(yg[q]))
-    # two-phase form: same v twice
+        check_op(op, w.batch, "sgmv", yg[q], what=f"grouped problem {q}")
+        assert np.array_equal(bits(yg[0]), bits(yg[q]))
     v1, v2 = new_v(32, 16, dev), new_v(32, 16, dev)
     m.lora_sgmv_shrink(v1, op.x, h, w.batch.seg_offsets, w.batch.seg_slot, 0)
     m.lora_sgmv_shrink(v2, op.x, h, w.batch.seg_offsets, w.batch.seg_slot, 0)
