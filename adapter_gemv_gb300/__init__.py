@@ -64,6 +64,8 @@ SIGNATURES = {
     "lora_sgmv": [_V, _I64, _V, _I64, _PP, _V, _V, _I32, _I32, _I32, _V, _V, _V],
     "lora_bgmv": [_V, _I64, _V, _I64, _PP, _V, _I32, _I32, _V, _V, _V],
     "lora_sgmv_grouped": [ctypes.POINTER(mlora_problem), _I32, _V, _V, _I32, _I32, _V, _V],
+    "lora_sgmv_grouped_prefetch": [ctypes.POINTER(mlora_problem), _I32, ctypes.POINTER(mlora_problem), _I32, _V, _V,
+                                   _I32, _I32, _V, _V],
 }
 
 
@@ -205,7 +207,8 @@ def lora_bgmv(y, x, pool, row_slot, layer, v_scratch, status=None, stream=None):
 
 
 class Group:
-    """A prepared lora_sgmv_grouped call: the problem array is built once and reused."""
+    """A prepared lora_sgmv_grouped call: the problem array is built once and reused.
+    set_next() attaches the L2 prefetch hint (lora_sgmv_grouped_prefetch)."""
 
     def __init__(self, problems: Sequence[tuple], seg_offsets, seg_slot, num_rows: int, status=None):
         """problems: (y, x, pool, layer, v_scratch) tuples sharing the rows' segments."""
@@ -225,15 +228,31 @@ class Group:
         self.off, self.slot = _i32(seg_offsets, "seg_offsets"), _i32(seg_slot, "seg_slot")
         self.nseg, self.M = int(seg_slot.numel()), int(num_rows)
         self.status = _i32(status, "status")
-        self.fn = lib().lora_sgmv_grouped
+        self.fn = lib().lora_sgmv_grouped_prefetch
+        self.next_arr, self.nnext = None, 0
+
+    def set_next(self, other: "Group"):
+        """Prefetch hint: `other` is the call that follows this one on the same stream."""
+        self.next_arr, self.nnext = (other.arr, other.n) if other is not None else (None, 0)
 
     def __call__(self, stream=None):
-        _check(self.fn(self.arr, self.n, self.off, self.slot, self.nseg, self.M, self.status, _stream(stream)))
+        _check(self.fn(self.arr, self.n, self.next_arr, self.nnext, self.off, self.slot, self.nseg, self.M,
+                       self.status, _stream(stream)))
 
 
 def lora_sgmv_grouped(problems, seg_offsets, seg_slot, status=None, stream=None):
     num_rows = int(problems[0][0].shape[0])
-    Group(problems, seg_offsets, seg_slot, num_rows, status)(stream)
+    g = Group(problems, seg_offsets, seg_slot, num_rows, status)
+    _check(lib().lora_sgmv_grouped(g.arr, g.n, g.off, g.slot, g.nseg, g.M, g.status, _stream(stream)))
+
+
+def lora_sgmv_grouped_prefetch(problems, next_problems, seg_offsets, seg_slot, status=None, stream=None):
+    """Grouped call plus the L2 prefetch hint for the call that follows (same rows)."""
+    num_rows = int(problems[0][0].shape[0])
+    g = Group(problems, seg_offsets, seg_slot, num_rows, status)
+    if next_problems:
+        g.set_next(Group(next_problems, seg_offsets, seg_slot, num_rows))
+    g(stream)
 
 
 def launch_count() -> int:

@@ -236,11 +236,13 @@ int lora_bgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool
   return run(mlora::MODE_FUSED, pool->dtype, d, stream);
 }
 
-int lora_sgmv_grouped(const mlora_problem *problems, int32_t num_problems, const int32_t *seg_offsets,
-                      const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t *dev_status,
-                      void *stream) {
+int lora_sgmv_grouped_prefetch(const mlora_problem *problems, int32_t num_problems, const mlora_problem *next,
+                               int32_t num_next, const int32_t *seg_offsets, const int32_t *seg_slot,
+                               int32_t num_segments, int32_t num_rows, int32_t *dev_status, void *stream) {
   if (!problems) return MLORA_ERR_NULL;
   if (num_problems < 1 || num_problems > MLORA_MAX_GROUP) return MLORA_ERR_SHAPE;
+  if (num_next < 0 || num_next > MLORA_MAX_GROUP) return MLORA_ERR_SHAPE;
+  if (num_next > 0 && !next) return MLORA_ERR_NULL;
   TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
   mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
   for (int q = 0; q < num_problems; ++q) {
@@ -253,8 +255,21 @@ int lora_sgmv_grouped(const mlora_problem *problems, int32_t num_problems, const
     d.prob[q] = problem(pb.pool, pb.layer, pb.x, pb.ldx, pb.y, pb.ldy, pb.v_scratch);
   }
   d.nprob = num_problems;
+  for (int q = 0; q < num_next; ++q) {
+    TRY(check_pool(next[q].pool, next[q].layer, true, true));
+    d.next_pool[q] = to_dev(next[q].pool);
+    d.next_layer[q] = next[q].layer;
+  }
+  d.nnext = num_next;
   if (num_rows == 0) return MLORA_OK;
   return run(mlora::MODE_FUSED, problems[0].pool->dtype, d, stream);
+}
+
+int lora_sgmv_grouped(const mlora_problem *problems, int32_t num_problems, const int32_t *seg_offsets,
+                      const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t *dev_status,
+                      void *stream) {
+  return lora_sgmv_grouped_prefetch(problems, num_problems, nullptr, 0, seg_offsets, seg_slot, num_segments, num_rows,
+                                    dev_status, stream);
 }
 
 const char *lora_error_string(int code) {

@@ -169,6 +169,29 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst_smem, const void *src_gm
       : "memory");
 }
 
+// Prefetch `bytes` (multiple of 16, 16-byte aligned) of global memory into L2, asynchronously:
+// nothing comes back to the SM and nothing is tracked. L2 is the point of coherence for the
+// SMs, so a line prefetched before another kernel writes it is updated by that write.
+__device__ __forceinline__ void prefetch_l2(const void *src_gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
+// 16-byte streaming load of data read once (no L1 allocation, evict-first in L2).
+__device__ __forceinline__ uint4 ldg_stream(const void *p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+
+// 16-byte load of data another kernel may have written (coherent path).
+__device__ __forceinline__ uint4 ldg_u4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
 // ---- clusters and distributed shared memory ------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -21,13 +21,6 @@ int sm_count() {
   return cached[dev];
 }
 
-// Split a chunk of `chunk` elements into equal blocks of at most `cap` elements, multiples of 8.
-int balanced_block(int chunk, int cap) {
-  cap = cap < 8 ? 8 : (cap & ~7);
-  const int nblk = (chunk + cap - 1) / cap;
-  return (((chunk + nblk - 1) / nblk) + 7) & ~7;
-}
-
 }  // namespace
 
 cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stream, bool pdl, int force_csplit) {
@@ -49,34 +42,37 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   p.tiles = (int32_t)tiles;
   const int64_t units = tiles * p.nprob;
 
-  // CTAs per tile: aim at two resident CTAs per SM over the whole launch, at least 128
-  // elements of the split dimension per CTA, at most 16 (a non-portable cluster above 8).
-  const int target = 2 * sm_count();
-  int cs = (int)((target + units - 1) / units);
+  // Rank rows per warp -> K elements per pass of A loads into registers.
+  const int jpw = r_alloc <= 16 ? 2 : r_alloc <= 32 ? 4 : r_alloc <= 64 ? 8 : 16;
+  const int kb = 256 * (16 / jpw);
+  // CTAs per tile (cs). Lower bounds: the CTA's slice of d_in is one pass of A loads, and its
+  // slice of B fits in shared memory (up to 176 KB). Otherwise about one CTA per SM for the
+  // launch, so most CTAs of the next launch (programmatic dependent launch) find room early;
+  // at least 256 elements of the split dimension per CTA; at most 16 per cluster.
+  const int sms = sm_count();
+  const int b_cap = 176 * 1024;
+  int cs_min = 1;
+  if (mode != MODE_EXPAND) cs_min = (d_in_max + kb - 1) / kb;
+  if (mode != MODE_SHRINK) {
+    const int need = (int)(((int64_t)r_alloc * d_out_max * 2 + b_cap - 1) / b_cap);
+    cs_min = cs_min > need ? cs_min : need;
+  }
+  int cs = (int)(sms / units);
+  cs = cs > cs_min ? cs : cs_min;
   const int split_dim = (mode == MODE_EXPAND) ? d_out_max : d_in_max;
-  const int max_cs = split_dim / 128 > 1 ? split_dim / 128 : 1;
-  cs = cs < 1 ? 1 : cs;
+  const int max_cs = split_dim / 256 > 1 ? split_dim / 256 : 1;
   cs = cs > max_cs ? max_cs : cs;
-  if (mode != MODE_EXPAND) cs = cs > (units * 8 >= target ? 8 : decode::MAX_CS) ? (units * 8 >= target ? 8 : decode::MAX_CS) : cs;
+  if (mode != MODE_EXPAND && cs > decode::MAX_CS) cs = decode::MAX_CS;
+  cs = cs < 1 ? 1 : cs;
   if (force_csplit > 0) cs = force_csplit;
   p.csplit = cs;
 
-  const int kchunk = ((d_in_max + cs - 1) / cs + 7) & ~7;
+  // B rows of the CTA's d_out slice go to shared memory when they fit.
   const int nchunk = ((d_out_max + cs - 1) / cs + 7) & ~7;
-  const int row_cap = (40 * 1024) / ((r_alloc + p.rt) * 2);  // elements per row in one stage
-  p.kb = (mode == MODE_EXPAND) ? 8 : balanced_block(kchunk, row_cap);
-  p.nb = (mode == MODE_SHRINK) ? 8 : balanced_block(nchunk, row_cap);
-  p.sk = (mode == MODE_EXPAND) ? 1 : ((kchunk + p.kb - 1) / p.kb < decode::MAX_STAGES ? (kchunk + p.kb - 1) / p.kb : decode::MAX_STAGES);
-  p.se = (mode == MODE_SHRINK) ? 1 : ((nchunk + p.nb - 1) / p.nb < decode::MAX_STAGES ? (nchunk + p.nb - 1) / p.nb : decode::MAX_STAGES);
-  if (mode == MODE_EXPAND) p.sk = 0;
-  if (mode == MODE_SHRINK) p.se = 0;
-  const int gcs = (mode == MODE_EXPAND) ? 1 : cs;
-  Layout L = Layout::make(gcs, p.rt, r_alloc, p.sk, p.kb, p.se, p.nb);
-  while (L.total > 227 * 1024 && (p.sk > 1 || p.se > 1)) {
-    if (p.sk >= p.se && p.sk > 1) --p.sk;
-    else --p.se;
-    L = Layout::make(gcs, p.rt, r_alloc, p.sk, p.kb, p.se, p.nb);
-  }
+  p.nb = (mode != MODE_SHRINK && (int64_t)r_alloc * nchunk * 2 <= b_cap) ? nchunk : 0;
+  p.kb = kb;
+  p.sk = p.se = 0;
+  const Layout L = Layout::make((mode == MODE_EXPAND) ? 1 : cs, p.rt, r_alloc, kb, p.nb);
   if (L.total > 227 * 1024) return cudaErrorInvalidConfiguration;
 
   const int64_t grid = units * cs;

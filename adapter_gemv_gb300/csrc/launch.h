@@ -32,6 +32,9 @@ struct ProblemDev {
 struct DecodeParams {
   ProblemDev prob[MLORA_MAX_GROUP];
   int32_t nprob;
+  PoolDev next_pool[MLORA_MAX_GROUP];  // L2 prefetch hint: pools and layers of the next call
+  int32_t next_layer[MLORA_MAX_GROUP];
+  int32_t nnext;
   const int32_t *seg_off, *seg_slot;  // SGMV (seg_off != nullptr)
   int32_t nseg;
   const int32_t *row_slot;  // BGMV

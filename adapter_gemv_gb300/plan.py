@@ -16,12 +16,13 @@ from . import MLORA_MAX_GROUP, Group, lora_set_programmatic_launch, make_pool
 
 
 class StepPlan:
-    def __init__(self, ops: Sequence, batch, status=None, programmatic: bool = True):
+    def __init__(self, ops: Sequence, batch, status=None, programmatic: bool = True, prefetch_next: bool = True):
         """ops: objects with .pool .layer .x .y (as workloads.Op); batch: .M .seg_offsets .seg_slot.
         programmatic: launch every call but the first with programmatic dependent launch. Safe
         because the kernel before each of those calls is this library's previous call, which
         writes none of the inputs a call reads before its wait (metadata, pool). The first call
-        keeps an ordinary dependency on whatever ran before the step."""
+        keeps an ordinary dependency on whatever ran before the step.
+        prefetch_next: each call carries the next call's problems as an L2 prefetch hint."""
         self.programmatic = programmatic
         self.handles = {}
         groups: List[List] = []
@@ -45,6 +46,9 @@ class StepPlan:
                 v = self.scratch[q].view(-1)[:batch.M * op.pool.r_max].view(batch.M, op.pool.r_max)  # row stride r_max
                 probs.append((op.y, op.x, h, op.layer, v))
             self.calls.append(Group(probs, batch.seg_offsets, batch.seg_slot, batch.M, status))
+        if prefetch_next:
+            for a, b in zip(self.calls, self.calls[1:]):
+                a.set_next(b)  # each call prefetches the next call's adapter rows into L2
         self.groups = groups
 
     def __call__(self, stream=None):

@@ -180,6 +180,19 @@ MLORA_API int lora_sgmv_grouped(const mlora_problem *problems, int32_t num_probl
                       const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t *dev_status,
                       void *stream);
 
+/* Same as lora_sgmv_grouped, plus a prefetch hint for a sequence of grouped calls over one batch
+ * (a decode step): `next` [num_next] lists the problems of the call that will follow on this
+ * stream, over the same rows and segments. While this call runs, its CTAs request into L2 the
+ * adapter rows (A and B of each row's slot) that those problems will read, so that the next
+ * call's weights stream from HBM during this one. Only the pools and layers of `next` are read;
+ * nothing is written for them and the result of this call does not depend on the hint
+ * (num_next == 0 makes it lora_sgmv_grouped). (No counterpart on the pages: an L2 prefetch
+ * schedule for GB300's 129 MB L2.) */
+MLORA_API int lora_sgmv_grouped_prefetch(const mlora_problem *problems, int32_t num_problems,
+                                         const mlora_problem *next, int32_t num_next, const int32_t *seg_offsets,
+                                         const int32_t *seg_slot, int32_t num_segments, int32_t num_rows,
+                                         int32_t *dev_status, void *stream);
+
 /* ---- utilities --------------------------------------------------------------------------- */
 
 /* Static text for a return code; for MLORA_ERR_CUDA it names the last CUDA error this thread saw. */
