@@ -137,6 +137,51 @@ int run(int mode, int dtype, const mlora::DecodeParams &d, void *stream) {
 }
 
 mlora::ProblemDev problem(const mlora_pool *pool, int32_t layer, const void *x, int64_t ldx, void *y, int64_t ldy,
+                          float *v);
+
+// SGMV with long segments: the full 128-row blocks of each segment on the tensor cores, the
+// remaining rows on the CUDA-core kernel (which skips the blocks). mode selects the phases.
+int run_sgmv(int mode, const mlora_pool *pool, int32_t layer, const void *x, int64_t ldx, void *y, int64_t ldy,
+             float *v, const int32_t *off, const int32_t *seg_slot, int32_t nseg, int32_t num_rows, int32_t *status,
+             void *stream) {
+  mlora::DecodeParams d = base_params(off, seg_slot, nseg, nullptr, num_rows, status);
+  d.prob[0] = problem(pool, layer, x, ldx, y, ldy, v);
+  d.nprob = 1;
+  if (mlora::tc_eligible(d.prob[0].pool, num_rows, nseg)) {
+    mlora::TcParams tp{};
+    tp.num_slots = pool->num_slots;
+    tp.num_layers = pool->num_layers;
+    tp.r_max = pool->r_max;
+    tp.d_in = pool->d_in;
+    tp.d_out = pool->d_out;
+    tp.layer = layer;
+    tp.rank = pool->rank;
+    tp.scale = pool->scale;
+    tp.seg_off = off;
+    tp.seg_slot = seg_slot;
+    tp.nseg = nseg;
+    tp.M = num_rows;
+    tp.v = v;
+    tp.y = static_cast<uint16_t *>(y);
+    tp.ldy = ldy;
+    tp.status = status;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (mode != mlora::MODE_EXPAND) {
+      const cudaError_t e = mlora::launch_tc_shrink(d.prob[0], tp, st);
+      if (e != cudaSuccess) return cuda_fail(e, "tensor-core shrink launch");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    if (mode != mlora::MODE_SHRINK) {
+      const cudaError_t e = mlora::launch_tc_expand(d.prob[0], tp, st);
+      if (e != cudaSuccess) return cuda_fail(e, "tensor-core expand launch");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    d.tc_rows = 128;
+  }
+  return run(mode, pool->dtype, d, stream);
+}
+
+mlora::ProblemDev problem(const mlora_pool *pool, int32_t layer, const void *x, int64_t ldx, void *y, int64_t ldy,
                           float *v) {
   mlora::ProblemDev q{};
   q.pool = to_dev(pool);
@@ -161,10 +206,8 @@ int lora_sgmv_shrink(float *v, const void *x, int64_t ldx, const mlora_pool *poo
   TRY(check_x(x, ldx, pool, num_rows));
   TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
-  mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
-  d.prob[0] = problem(pool, layer, x, ldx, nullptr, 0, v);
-  d.nprob = 1;
-  return run(mlora::MODE_SHRINK, pool->dtype, d, stream);
+  return run_sgmv(mlora::MODE_SHRINK, pool, layer, x, ldx, nullptr, 0, v, seg_offsets, seg_slot, num_segments,
+                  num_rows, dev_status, stream);
 }
 
 int lora_sgmv_expand(void *y, int64_t ldy, const float *v, const mlora_pool *pool, const int32_t *seg_offsets,
@@ -175,10 +218,8 @@ int lora_sgmv_expand(void *y, int64_t ldy, const float *v, const mlora_pool *poo
   TRY(check_y(y, ldy, pool, num_rows));
   TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
-  mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
-  d.prob[0] = problem(pool, layer, nullptr, 0, y, ldy, const_cast<float *>(v));
-  d.nprob = 1;
-  return run(mlora::MODE_EXPAND, pool->dtype, d, stream);
+  return run_sgmv(mlora::MODE_EXPAND, pool, layer, nullptr, 0, y, ldy, const_cast<float *>(v), seg_offsets, seg_slot,
+                  num_segments, num_rows, dev_status, stream);
 }
 
 int lora_bgmv_shrink(float *v, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
@@ -216,10 +257,8 @@ int lora_sgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool
   TRY(check_y(y, ldy, pool, num_rows));
   TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
-  mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
-  d.prob[0] = problem(pool, layer, x, ldx, y, ldy, v_scratch);
-  d.nprob = 1;
-  return run(mlora::MODE_FUSED, pool->dtype, d, stream);
+  return run_sgmv(mlora::MODE_FUSED, pool, layer, x, ldx, y, ldy, v_scratch, seg_offsets, seg_slot, num_segments,
+                  num_rows, dev_status, stream);
 }
 
 int lora_bgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,

@@ -40,9 +40,30 @@ struct DecodeParams {
   const int32_t *row_slot;  // BGMV
   int32_t M;
   int32_t *status;
+  int32_t tc_rows;  // > 0: the first floor(len / tc_rows) * tc_rows rows of each segment are done
+                    // by the tensor-core kernels; these kernels take only the rest
   // chosen by the launcher
   int32_t rt, tiles, csplit, kb, nb, sk, se, r_alloc;
 };
+
+// Tensor-core path for the full 128-row blocks of long SGMV segments (prefill_tc.cu).
+struct TcParams {
+  int32_t num_slots, num_layers, r_max, d_in, d_out, layer;
+  const int32_t *rank;
+  const float *scale;
+  const int32_t *seg_off, *seg_slot;
+  int32_t nseg, M;
+  float *v;  // [M][r_max] fp32: written by the shrink, read by the expand
+  uint16_t *y;
+  int64_t ldy;
+  int32_t *status;
+  // chosen by the launcher
+  int32_t rpad, ksplit, tiles, nper, nblk_total, tmem_cols;
+};
+
+bool tc_eligible(const PoolDev &pool, int num_rows, int nseg);
+cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stream);
+cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stream);
 
 // CUDA-core path for decode-sized tiles (decode_launch.cu chooses the split and the stages;
 // decode_{shrink,expand,fused}.cu hold the kernels). force_csplit > 0 overrides the split.

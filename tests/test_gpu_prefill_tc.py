@@ -1,0 +1,80 @@
+"""Tensor-core prefill path against the oracle: long SGMV segments whose full 128-row blocks run
+on tcgen05 kernels and whose tails run on the CUDA-core kernels. Segment lengths around the
+128-row boundary, empty and -1 segments, K and N extents that are not multiples of the tile,
+ranks below the padded rank (padding rows hold NaN), every row compared."""
+import numpy as np
+import pytest
+import torch
+
+import adapter_gemv_gb300 as m
+import workloads as W
+from gpu_util import check_op, new_v
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import os
+    if not os.path.exists(m.LIB_PATH):
+        from adapter_gemv_gb300 import build
+        build.build()
+    return torch.device("cuda:0")
+
+
+CASES = [
+    # r_max, ranks, d_in, d_out, segment lengths, segment slots
+    (16, [16, 8, 1, 16], 264, 200, [128, 300, 0, 129, 5, 256], [0, 1, 2, -1, 3, 1]),
+    (64, [64, 64, 33, 64], 5120, 640, [255, 130, 384], [2, 0, 1]),
+    (40, [40, 17, 40], 512, 4104, [200, 128, 129], [1, 0, 2]),
+    (128, [128, 96], 1032, 1104, [256, 131], [0, 1]),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"r{c[0]}-{c[2]}x{c[3]}-M{sum(c[4])}")
+@pytest.mark.parametrize("mode", ["two_phase", "fused"])
+def test_prefill_tensor_core_path(dev, case, mode):
+    r_max, ranks, d_in, d_out, lens, slots = case
+    g = W.generator(7, dev)
+    pool = W.stacked_pool(num_slots=len(ranks), num_layers=2, r_max=r_max, d_in=d_in, d_out=d_out,
+                          dtype=torch.bfloat16, gen=g, device=dev, ranks=ranks)
+    batch = W.batch_from_segments(lens, slots).to(dev)
+    M = batch.M
+    x = W.normal((M, d_in), 1.0, torch.bfloat16, g, dev)
+    y0 = W.uniform((M, d_out), -1, 1, torch.bfloat16, g, dev)
+    op = W.Op("p", pool, 1, x, y0)
+    h = m.make_pool(pool)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = y0.clone()
+    v = new_v(M, r_max, dev)
+    before = m.launch_count()
+    if mode == "two_phase":
+        m.lora_sgmv_shrink(v, x, h, batch.seg_offsets, batch.seg_slot, 1, st)
+        m.lora_sgmv_expand(y, v, h, batch.seg_offsets, batch.seg_slot, 1, st)
+        launches = 4  # tensor-core shrink + tails, tensor-core expand + tails
+    else:
+        m.lora_sgmv(y, x, h, batch.seg_offsets, batch.seg_slot, 1, v, st)
+        launches = 3
+    torch.cuda.synchronize()
+    assert m.launch_count() - before == launches, "the tensor-core path did not run"
+    assert st.item() == 0
+    check_op(op, batch, "sgmv", y, v if mode == "two_phase" else None, what=f"tc {mode}")
+
+
+def test_prefill_bad_offsets_launch_tc_but_write_nothing(dev):
+    g = W.generator(8, dev)
+    pool = W.stacked_pool(num_slots=2, num_layers=1, r_max=16, d_in=128, d_out=128, dtype=torch.bfloat16, gen=g,
+                          device=dev)
+    M = 512
+    x = W.normal((M, 128), 1.0, torch.bfloat16, g, dev)
+    y = W.uniform((M, 128), -1, 1, torch.bfloat16, g, dev)
+    y_ref = y.clone()
+    off = torch.tensor([0, 256, 500], dtype=torch.int32, device=dev)  # ends at 500 != 512
+    slot = torch.tensor([0, 1], dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    m.lora_sgmv(y, x, m.make_pool(pool), off, slot, 0, new_v(M, 16, dev), st)
+    torch.cuda.synchronize()
+    assert st.item() == m.STATUS_BAD_OFFSETS
+    assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
