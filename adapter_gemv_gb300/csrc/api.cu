@@ -139,8 +139,8 @@ int run(int mode, int dtype, const mlora::DecodeParams &d, void *stream) {
 mlora::ProblemDev problem(const mlora_pool *pool, int32_t layer, const void *x, int64_t ldx, void *y, int64_t ldy,
                           float *v);
 
-// SGMV with long segments: the full 128-row blocks of each segment on the tensor cores, the
-// remaining rows on the CUDA-core kernel (which skips the blocks). mode selects the phases.
+// SGMV with long segments: segments of at least kTcMinRows rows on the tensor cores (128-row
+// blocks, the last one masked), shorter ones on the CUDA-core kernel. mode selects the phases.
 int run_sgmv(int mode, const mlora_pool *pool, int32_t layer, const void *x, int64_t ldx, void *y, int64_t ldy,
              float *v, const int32_t *off, const int32_t *seg_slot, int32_t nseg, int32_t num_rows, int32_t *status,
              void *stream) {
@@ -176,7 +176,7 @@ int run_sgmv(int mode, const mlora_pool *pool, int32_t layer, const void *x, int
       if (e != cudaSuccess) return cuda_fail(e, "tensor-core expand launch");
       g_launches.fetch_add(1, std::memory_order_relaxed);
     }
-    d.tc_rows = 128;
+    d.tc_min = mlora::kTcMinRows;
   }
   return run(mode, pool->dtype, d, stream);
 }

@@ -99,11 +99,7 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
             lo = scan[q];
             len = scan[q + 1] - lo;
             if (len < 0 || lo < 0 || scan[q + 1] > p.M) bad = 1;
-            if (p.tc_rows > 0 && len > 0) {  // full tensor-core blocks are done elsewhere
-              const int32_t covered = (len / p.tc_rows) * p.tc_rows;
-              lo += covered;
-              len -= covered;
-            }
+            if (p.tc_min > 0 && len >= p.tc_min) len = 0;  // a tensor-core kernel does this segment
           }
           const int32_t nt = (q < cnt && len > 0) ? (len + p.rt - 1) / p.rt : 0;
           int32_t incl = nt;

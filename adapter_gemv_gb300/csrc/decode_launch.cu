@@ -37,7 +37,12 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   const bool sgmv = p.seg_off != nullptr;
   const bool multi = sgmv && p.M >= 2 * (p.nseg > 0 ? p.nseg : 1);
   p.rt = multi ? (r_alloc <= 64 ? 8 : 4) : 1;
-  const int64_t tiles = !sgmv ? (int64_t)p.M : (p.rt == 1 ? (int64_t)p.M : (int64_t)p.nseg + (p.M + p.rt - 1) / p.rt);
+  int64_t tiles = !sgmv ? (int64_t)p.M : (p.rt == 1 ? (int64_t)p.M : (int64_t)p.nseg + (p.M + p.rt - 1) / p.rt);
+  if (sgmv && p.tc_min > 0) {
+    // only segments shorter than tc_min rows are left for these kernels
+    const int64_t per_seg = (p.tc_min - 1 + p.rt - 1) / p.rt;
+    tiles = tiles < (int64_t)p.nseg * per_seg ? tiles : (int64_t)p.nseg * per_seg;
+  }
   if (tiles <= 0) return cudaSuccess;
   p.tiles = (int32_t)tiles;
   const int64_t units = tiles * p.nprob;

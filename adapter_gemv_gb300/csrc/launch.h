@@ -40,8 +40,8 @@ struct DecodeParams {
   const int32_t *row_slot;  // BGMV
   int32_t M;
   int32_t *status;
-  int32_t tc_rows;  // > 0: the first floor(len / tc_rows) * tc_rows rows of each segment are done
-                    // by the tensor-core kernels; these kernels take only the rest
+  int32_t tc_min;  // > 0: segments of at least tc_min rows are done by the tensor-core kernels;
+                   // these kernels take only the shorter segments
   // chosen by the launcher
   int32_t rt, tiles, csplit, kb, nb, sk, se, r_alloc;
 };
@@ -57,9 +57,12 @@ struct TcParams {
   uint16_t *y;
   int64_t ldy;
   int32_t *status;
+  int32_t tc_min;  // segments of at least this many rows are this path's
   // chosen by the launcher
   int32_t rpad, ksplit, tiles, nper, nblk_total, tmem_cols;
 };
+
+constexpr int kTcMinRows = 32;
 
 bool tc_eligible(const PoolDev &pool, int num_rows, int nseg);
 cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stream);

@@ -31,17 +31,17 @@ namespace {
 constexpr int BM = 128;      // rows per tile (MMA M)
 constexpr int BK = 64;       // K elements per stage (one 128-byte swizzle row)
 constexpr int STAGES = 4;    // shrink ring depth
-constexpr int BN = 128;      // expand: columns per N block (MMA N)
 constexpr int NTHREADS = 128;
 constexpr int SCAN_CAP = 512;
 
 struct TcTile {
-  int32_t row0, slot, rank, skip, bad;
+  int32_t row0, nr, slot, rank, skip, bad;
   float scale;
 };
 
-// Tile t = the t-th full 128-row block, walking the segments in order (each contributes
-// floor(len / 128) blocks). Whole block participates; row metadata only.
+// Tile t = the t-th 128-row block, walking the segments in order: a segment of at least
+// p.tc_min rows contributes ceil(len / 128) blocks (the last one may be partial: nr < 128);
+// shorter segments belong to the CUDA-core kernels. Whole block participates; row metadata only.
 __device__ void resolve_tc_tile(const TcParams &p, int t, TcTile *ti, int32_t *scan) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -67,7 +67,7 @@ __device__ void resolve_tc_tile(const TcParams &p, int t, TcTile *ti, int32_t *s
           len = scan[q + 1] - lo;
           if (len < 0 || lo < 0 || scan[q + 1] > p.M) bad = 1;
         }
-        const int32_t nt = (q < cnt && len > 0) ? len / BM : 0;
+        const int32_t nt = (q < cnt && len >= p.tc_min && len > 0) ? (len + BM - 1) / BM : 0;
         int32_t incl = nt;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -78,6 +78,7 @@ __device__ void resolve_tc_tile(const TcParams &p, int t, TcTile *ti, int32_t *s
         const bool mine = q < cnt && t >= excl && t < excl + nt;
         if (!found && mine) {
           ti->row0 = lo + (t - excl) * BM;
+          ti->nr = min(BM, len - (t - excl) * BM);
           ti->slot = scan[SCAN_CAP + 1 + q];
         }
         found |= __any_sync(0xffffffffu, mine);
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
   resolve_tc_tile(p, t, ti, scan);
   if (c == 0 && tid == 0 && ti->bad) report(p.status, ti->bad);
   const bool active = !ti->skip;
-  const int row0 = ti->row0, s = ti->slot, rank = ti->rank;
+  const int row0 = ti->row0, nr = ti->nr, s = ti->slot, rank = ti->rank;
   const int kb_total = (p.d_in + BK - 1) / BK;
   const int kb_per = (kb_total + ks - 1) / ks;
   const int kb0 = min((int)c * kb_per, kb_total), kb1 = min(kb0 + kb_per, kb_total);
@@ -237,10 +238,12 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
         for (int e = 0; e < 16; ++e) vals[e] = 0.f;
       }
       if (ks == 1) {
+        if (m < nr) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int j = c16 * 16 + e;
-          if (j < rank) p.v[(int64_t)(row0 + m) * p.r_max + j] = vals[e];
+          for (int e = 0; e < 16; ++e) {
+            const int j = c16 * 16 + e;
+            if (j < rank) p.v[(int64_t)(row0 + m) * p.r_max + j] = vals[e];
+          }
         }
       } else {
 #pragma unroll
@@ -251,10 +254,11 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
   if (ks > 1) {
     cluster_sync();
     if (active && !timed_out) {
-      // CTA c sums rows [c * 128 / ks, (c + 1) * 128 / ks) over the cluster, in rank order
-      const int rows_per = BM / ks;
-      for (int e = tid; e < rows_per * rank; e += NTHREADS) {
-        const int mm = (int)c * rows_per + e / rank, j = e % rank;
+      // CTA c sums rows [c * rp, min(128, (c + 1) * rp)) over the cluster, in rank order
+      const int rp = (BM + ks - 1) / ks;
+      const int m_lo = min((int)c * rp, nr), m_hi = min(m_lo + rp, nr);
+      for (int e = tid; e < (m_hi - m_lo) * rank; e += NTHREADS) {
+        const int mm = m_lo + e / rank, j = e % rank;
         float sum = 0.f;
         for (int q = 0; q < ks; ++q) sum += dsmem_ld_f32(dsmem_addr(&red[mm * p.rpad + j], q));
         p.v[(int64_t)(row0 + mm) * p.r_max + j] = sum;
@@ -271,30 +275,35 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
 // ------------------------------------------------------------------------------------------
 // expand
 
+// Shared memory: V hi / lo, then two pipeline buffers, each with the B rows of one 64-column
+// block (one MN atom: rpad K rows x 128 B) and the y tile of that block (128 rows x 128 B).
 struct ExpandSmem {
-  int v_off, b_off, b_buf, bar_off, total;
+  int v_off, buf_off, buf_bytes, b_in_buf, bar_off, total;
   __host__ __device__ static ExpandSmem make(int rpad) {
     ExpandSmem L;
     const int katoms = (rpad + BK - 1) / BK;
-    L.v_off = 0;                                     // V hi, V lo: [2][katoms][128 rows x 128 B]
-    L.b_off = 2 * katoms * BM * 128;
-    L.b_buf = 2 * rpad * 128;                        // one N block: 2 MN atoms x rpad K rows x 128 B
-    L.bar_off = L.b_off + 2 * ((L.b_buf + 1023) & ~1023);
+    L.v_off = 0;
+    L.buf_off = 2 * katoms * BM * 128;
+    L.b_in_buf = BM * 128;                                   // y tile first (16 KB), then B rows
+    L.buf_bytes = (L.b_in_buf + rpad * 128 + 1023) & ~1023;
+    L.bar_off = L.buf_off + 2 * L.buf_bytes;
     L.total = L.bar_off + 1024 + (2 * SCAN_CAP + 1) * 4 + 1024;
     return L;
   }
 };
 
+constexpr int EBN = 64;  // expand: columns per pipeline block (MMA N)
+
 template <int DT>
 __global__ void __launch_bounds__(NTHREADS) tc_expand_kernel(const __grid_constant__ CUtensorMap tm_b,
+                                                             const __grid_constant__ CUtensorMap tm_y,
                                                              const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   const ExpandSmem L = ExpandSmem::make(p.rpad);
   const int katoms = (p.rpad + BK - 1) / BK;
-  const int bbuf = (L.b_buf + 1023) & ~1023;
-  uint64_t *bfull = reinterpret_cast<uint64_t *>(smem + L.bar_off);  // [2]
-  uint64_t *accbar = bfull + 2;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);  // [2]: B rows + y tile landed
+  uint64_t *accbar = full + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accbar + 1);
   TcTile *ti = reinterpret_cast<TcTile *>(smem + L.bar_off + 256);
   int32_t *scan = reinterpret_cast<int32_t *>(smem + L.bar_off + 1024);
@@ -305,13 +314,14 @@ __global__ void __launch_bounds__(NTHREADS) tc_expand_kernel(const __grid_consta
   const int nb_end = min(nb_begin + p.nper, p.nblk_total);
 
   if (tid == 0) {
-    mbar_init(&bfull[0], 1);
-    mbar_init(&bfull[1], 1);
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
     mbar_init(accbar, 1);
     mbar_fence_init();
     tc::tma_prefetch_desc(&tm_b);
+    tc::tma_prefetch_desc(&tm_y);
   }
-  if (warp == 0) tc::tmem_alloc(tmem_slot, BN);
+  if (warp == 0) tc::tmem_alloc(tmem_slot, EBN);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -320,37 +330,50 @@ __global__ void __launch_bounds__(NTHREADS) tc_expand_kernel(const __grid_consta
   resolve_tc_tile(p, t, ti, scan);
   if (blockIdx.x == 0 && tid == 0 && ti->bad) report(p.status, ti->bad);
   const bool active = !ti->skip && nb_begin < nb_end;
-  const int row0 = ti->row0, s = ti->slot, rank = ti->rank;
+  const int row0 = ti->row0, nr = ti->nr, s = ti->slot, rank = ti->rank;
   const float scale = ti->scale;
+  const bool full_tile = nr == BM;  // a partial tile writes its rows with plain stores: the
+                                    // rows past nr belong to another segment
   const int brow = (s * p.num_layers + p.layer) * p.r_max;
-  const uint32_t block_tx = (uint32_t)(2 * p.rpad * 128);
-  const uint32_t idesc = tc::idesc_f16(DT == MLORA_BF16, false, true, BM, BN);
+  const uint32_t block_tx = (uint32_t)(p.rpad * 128 + BM * 128);
+  const uint32_t idesc = tc::idesc_f16(DT == MLORA_BF16, false, true, BM, EBN);
   int timed_out = 0;
 
-  auto issue_b = [&](int nb) {  // both 64-column MN atoms of N block nb
-    uint8_t *dst = smem + L.b_off + (nb & 1) * bbuf;
-    mbar_arrive_expect_tx(&bfull[nb & 1], block_tx);
-    tc::tma_load_2d(dst, &tm_b, nb * BN, brow, &bfull[nb & 1]);
-    tc::tma_load_2d(dst + p.rpad * 128, &tm_b, nb * BN + 64, brow, &bfull[nb & 1]);
+  auto buf = [&](int nb) { return smem + L.buf_off + (nb & 1) * L.buf_bytes; };
+  auto issue = [&](int nb) {  // one lane: y tile and B rows of block nb
+    uint8_t *dst = buf(nb);
+    mbar_arrive_expect_tx(&full[nb & 1], block_tx);
+    tc::tma_load_2d(dst, &tm_y, nb * EBN, row0, &full[nb & 1]);
+    tc::tma_load_2d(dst + L.b_in_buf, &tm_b, nb * EBN, brow, &full[nb & 1]);
   };
 
   if (active) {
     if (warp == 0) {
       if (lane == 0) {
-        issue_b(nb_begin);
-        if (nb_begin + 1 < nb_end) issue_b(nb_begin + 1);
+        issue(nb_begin);
+        if (nb_begin + 1 < nb_end) issue(nb_begin + 1);
       }
       __syncwarp();
     }
     // V hi / lo in the K-major 128-byte-swizzle layout: thread m owns row m
     const int m = tid;
-    const float *vrow = p.v + (int64_t)(row0 + m) * p.r_max;
+    const float *vrow = p.v + (int64_t)(row0 + (m < nr ? m : 0)) * p.r_max;
+    const bool vec = ((p.r_max & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.v) & 15) == 0);
     for (int c8 = 0; c8 < katoms * 8; ++c8) {  // 16-byte chunks of 8 K elements
       float f[8], hi[8], lo[8];
+      if (m >= nr) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j = c8 * 8 + e;
-        f[e] = (j < rank) ? vrow[j] : 0.f;
+        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+      } else if (vec && c8 * 8 + 8 <= rank) {
+        const float4 a = *reinterpret_cast<const float4 *>(vrow + c8 * 8);
+        const float4 b = *reinterpret_cast<const float4 *>(vrow + c8 * 8 + 4);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = c8 * 8 + e;
+          f[e] = (j < rank) ? vrow[j] : 0.f;
+        }
       }
       const uint4 h = pack8<DT>(f);
       unpack8<DT>(h, hi);
@@ -367,79 +390,86 @@ __global__ void __launch_bounds__(NTHREADS) tc_expand_kernel(const __grid_consta
   __syncthreads();
 
   for (int nb = nb_begin; active && nb < nb_end && !timed_out; ++nb) {
-    const int buf = nb & 1;
-    uint8_t *bsm = smem + L.b_off + buf * bbuf;
-    const int okb = mbar_wait(&bfull[buf], (uint32_t)((nb - nb_begin) >> 1) & 1u) ? 1 : 0;
+    uint8_t *bb = buf(nb);
+    uint8_t *ys = bb;                 // y tile: 128 rows x 64 columns, 128-byte swizzle
+    uint8_t *bs = bb + L.b_in_buf;    // B rows: rpad K rows x 64 columns (one MN atom)
+    const int okb = mbar_wait(&full[nb & 1], (uint32_t)((nb - nb_begin) >> 1) & 1u) ? 1 : 0;
     timed_out = __syncthreads_or(!okb);
     if (timed_out) break;
     if (rank < p.rpad) {
-      // rows rank..rpad-1 of B are padding (possibly NaN): zero them in both MN atoms
-      for (int e = tid; e < 2 * (p.rpad - rank) * 8; e += NTHREADS) {
-        const int atom = e / ((p.rpad - rank) * 8), rem = e % ((p.rpad - rank) * 8);
-        const int j = rank + rem / 8, ch = rem % 8;
-        *reinterpret_cast<uint4 *>(bsm + atom * p.rpad * 128 + j * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-      }
+      // rows rank..rpad-1 of B are padding (possibly NaN): zero them
+      for (int e = tid; e < (p.rpad - rank) * 8; e += NTHREADS)
+        *reinterpret_cast<uint4 *>(bs + (rank + e / 8) * 128 + (e % 8) * 16) = make_uint4(0, 0, 0, 0);
       tc::fence_proxy_async();
       __syncthreads();
     }
     if (warp == 1) {
       if (lane == 0) {
-      tc::tc_fence_after();
-      const int ksteps = p.rpad / 16;
-      for (int part = 0; part < 2; ++part) {  // V hi, then V lo
-        for (int kk = 0; kk < ksteps; ++kk) {
-          const uint8_t *va = smem + L.v_off + part * katoms * BM * 128 + (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          const uint64_t da = tc::smem_desc_sw128(va, 16, 1024);
-          const uint64_t db = tc::smem_desc_sw128(bsm + kk * 16 * 128, (uint32_t)(p.rpad * 128), 1024);
-          tc::mma_f16(tmem, da, db, idesc, (part > 0 || kk > 0) ? 1u : 0u);
+        tc::tc_fence_after();
+        const int ksteps = p.rpad / 16;
+        for (int part = 0; part < 2; ++part) {  // V hi, then V lo
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint8_t *va = smem + L.v_off + part * katoms * BM * 128 + (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+            const uint64_t da = tc::smem_desc_sw128(va, 16, 1024);
+            const uint64_t db = tc::smem_desc_sw128(bs + kk * 16 * 128, 16, 1024);
+            tc::mma_f16(tmem, da, db, idesc, (part > 0 || kk > 0) ? 1u : 0u);
+          }
         }
-      }
-      tc::mma_commit(accbar);
+        tc::mma_commit(accbar);
       }
       __syncwarp();
     }
-    // y of this thread's row for the block, requested while the MMAs run
-    const int m = tid, n0 = nb * BN;
-    uint16_t *yrow = p.y + (int64_t)(row0 + m) * p.ldy;
-    uint4 yv[BN / 8];
-#pragma unroll
-    for (int q = 0; q < BN / 8; ++q)
-      if (n0 + q * 8 < p.d_out) yv[q] = ldg_u4(yrow + n0 + q * 8);
     const int oka = mbar_wait(accbar, (uint32_t)(nb - nb_begin) & 1u) ? 1 : 0;
     timed_out = __syncthreads_or(!oka);
     if (timed_out) break;
     tc::tc_fence_after();
-    if (warp == 0) {
-      if (lane == 0 && nb + 2 < nb_end) issue_b(nb + 2);  // the MMAs are done with this buffer
-      __syncwarp();
-    }
+    // epilogue: row m of the y tile in shared memory += scale * D, rounded once
+    const int m = tid;
 #pragma unroll
-    for (int c16 = 0; c16 < BN / 16; ++c16) {
+    for (int c16 = 0; c16 < EBN / 16; ++c16) {
       float d[16];
       tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c16 * 16), d);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int q = c16 * 2 + h;
-        if (n0 + q * 8 < p.d_out) {
-          float yf[8];
-          unpack8<DT>(yv[q], yf);
+        const int ch = c16 * 2 + h;  // 16-byte chunk of the 128-byte row
+        uint4 *cell = reinterpret_cast<uint4 *>(ys + m * 128 + ((ch ^ (m & 7)) << 4));
+        float yf[8];
+        unpack8<DT>(*cell, yf);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) yf[e] = fmaf(scale, d[h * 8 + e], yf[e]);
-          *reinterpret_cast<uint4 *>(yrow + n0 + q * 8) = pack8<DT>(yf);
+        for (int e = 0; e < 8; ++e) yf[e] = fmaf(scale, d[h * 8 + e], yf[e]);
+        if (full_tile) {
+          *cell = pack8<DT>(yf);
+        } else if (m < nr && nb * EBN + ch * 8 < p.d_out) {
+          *reinterpret_cast<uint4 *>(p.y + (int64_t)(row0 + m) * p.ldy + nb * EBN + ch * 8) = pack8<DT>(yf);
         }
       }
     }
+    tc::fence_proxy_async();
     tc::tc_fence_before();
-    __syncthreads();  // TMEM and the B buffer are reused by the next block
+    __syncthreads();  // the tile is complete; TMEM may be overwritten
+    if (warp == 0) {
+      if (lane == 0) {
+        if (full_tile) tc::tma_store_2d(&tm_y, nb * EBN, row0, ys);  // columns past d_out are clipped
+        tc::bulk_commit_group();
+        if (nb + 2 < nb_end) {
+          tc::bulk_wait_group_read<0>();  // this buffer's store has read the tile
+          issue(nb + 2);
+        }
+      }
+      __syncwarp();
+    }
+  }
+  if (warp == 0) {
+    if (lane == 0) tc::bulk_wait_group_all();  // stores complete before the shared memory goes away
+    __syncwarp();
   }
   if (timed_out) {
-    // copies still in flight land before the shared memory is released
-    (void)mbar_wait(&bfull[0], 0, 100000000ull);
+    (void)mbar_wait(&full[0], 0, 100000000ull);
     if (tid == 0) report(p.status, MLORA_STATUS_TIMEOUT);
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, BN);
+  if (warp == 0) tc::tmem_dealloc(tmem, EBN);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -495,6 +525,9 @@ cudaError_t set_smem(K kern, size_t smem) {
 
 }  // namespace
 
+// Segments of at least this many rows run on the tensor cores (last block masked).
+constexpr int TC_MIN_ROWS = kTcMinRows;
+
 bool tc_eligible(const PoolDev &pool, int num_rows, int nseg) {
   return pool.kind == MLORA_POOL_STACKED && pool.dtype == MLORA_BF16 && pool.r_max <= 128 && num_rows >= BM &&
          (int64_t)num_rows >= (int64_t)64 * (nseg > 0 ? nseg : 1) && encoder() != nullptr;
@@ -504,10 +537,12 @@ cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stre
   const PoolDev &pl = pr.pool;
   p.rpad = (pl.r_max + 15) & ~15;
   p.tmem_cols = p.rpad <= 32 ? 32 : p.rpad <= 64 ? 64 : 128;
-  p.tiles = p.M / BM;
+  p.tc_min = TC_MIN_ROWS;
+  p.tiles = p.M / BM + p.nseg;  // >= sum over long segments of ceil(len / 128)
   if (p.tiles <= 0) return cudaSuccess;
   const int kb_total = (pl.d_in + BK - 1) / BK;
-  int ks = sm_count_tc() / p.tiles;
+  const int real_tiles = p.M / BM > 0 ? p.M / BM : 1;
+  int ks = (2 * sm_count_tc() + real_tiles / 2) / real_tiles;  // about two CTAs per SM
   ks = ks < 1 ? 1 : ks > 4 ? 4 : ks;
   ks = ks > kb_total ? kb_total : ks;
   p.ksplit = ks;
@@ -537,19 +572,21 @@ cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stre
 cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stream) {
   const PoolDev &pl = pr.pool;
   p.rpad = (pl.r_max + 15) & ~15;
-  p.tiles = p.M / BM;
+  p.tc_min = TC_MIN_ROWS;
+  p.tiles = p.M / BM + p.nseg;
   if (p.tiles <= 0) return cudaSuccess;
-  p.nblk_total = (pl.d_out + BN - 1) / BN;
-  p.nper = 4;
-  CUtensorMap tm_b;
+  p.nblk_total = (pl.d_out + EBN - 1) / EBN;
+  p.nper = 8;
+  CUtensorMap tm_b, tm_y;
   if (!encode_2d(&tm_b, pl.dtype, pl.b, pl.d_out, (int64_t)pl.num_slots * pl.num_layers * pl.r_max, pl.d_out, p.rpad))
     return cudaErrorInvalidValue;
+  if (!encode_2d(&tm_y, pl.dtype, pr.y, pl.d_out, p.M, pr.ldy, BM)) return cudaErrorInvalidValue;
   const size_t smem = ExpandSmem::make(p.rpad).total;
   auto kern = tc_expand_kernel<MLORA_BF16>;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((p.nblk_total + p.nper - 1) / p.nper, p.tiles, 1);
-  kern<<<grid, NTHREADS, smem, stream>>>(tm_b, p);
+  kern<<<grid, NTHREADS, smem, stream>>>(tm_b, tm_y, p);
   return cudaGetLastError();
 }
 

@@ -30,6 +30,10 @@ CASES = [
     (64, [64, 64, 33, 64], 5120, 640, [255, 130, 384], [2, 0, 1]),
     (40, [40, 17, 40], 512, 4104, [200, 128, 129], [1, 0, 2]),
     (128, [128, 96], 1032, 1104, [256, 131], [0, 1]),
+    # segments around the 32-row threshold: partial tensor-core tiles next to CUDA-core segments
+    (16, [16, 5, 16], 320, 328, [31, 32, 33, 64, 127, 200, 1], [0, 1, 2, 0, 1, 2, -1]),
+    # enough 128-row blocks that the K split is 3 (rows do not divide evenly over the cluster)
+    (16, [16, 16], 256, 136, [128 * 60 + 7, 128 * 41], [0, 1]),
 ]
 
 
