@@ -26,7 +26,8 @@ MLORA_POOL_STACKED, MLORA_POOL_PAGED = 0, 1
 MLORA_MAX_GROUP = 8
 MLORA_MAX_RANK = 128
 STATUS_BAD_OFFSETS, STATUS_BAD_SLOT, STATUS_BAD_RANK, STATUS_BAD_PAGE, STATUS_TIMEOUT = 1, 2, 4, 8, 16
-ERR_NULL, ERR_DTYPE, ERR_SHAPE, ERR_ALIGN, ERR_POOL, ERR_CUDA = -1, -2, -3, -4, -5, -6
+ERR_NULL, ERR_DTYPE, ERR_SHAPE, ERR_ALIGN, ERR_POOL, ERR_CUDA, ERR_TOO_LARGE = -1, -2, -3, -4, -5, -6, -7
+NOALLOC_MAX_FLOATS = 1 << 20
 
 _DT = {torch.bfloat16: MLORA_BF16, torch.float16: MLORA_FP16}
 
@@ -63,6 +64,7 @@ SIGNATURES = {
     "lora_bgmv_expand": [_V, _I64, _V, _PP, _V, _I32, _I32, _V, _V],
     "lora_sgmv": [_V, _I64, _V, _I64, _PP, _V, _V, _I32, _I32, _I32, _V, _V, _V],
     "lora_bgmv": [_V, _I64, _V, _I64, _PP, _V, _I32, _I32, _V, _V, _V],
+    "lora_sgmv_noalloc": [_V, _I64, _V, _I64, _PP, _V, _V, _I32, _I32, _I32, _V, _V],
     "lora_sgmv_grouped": [ctypes.POINTER(mlora_problem), _I32, _V, _V, _I32, _I32, _V, _V],
     "lora_sgmv_grouped_prefetch": [ctypes.POINTER(mlora_problem), _I32, ctypes.POINTER(mlora_problem), _I32, _V, _V,
                                    _I32, _I32, _V, _V],
@@ -197,6 +199,17 @@ def lora_sgmv(y, x, pool, seg_offsets, seg_slot, layer, v_scratch, status=None, 
                            _rows(x, "x", h.dtype), h.ref, _i32(seg_offsets, "seg_offsets"),
                            _i32(seg_slot, "seg_slot"), int(seg_slot.numel()), int(y.shape[0]), int(layer),
                            _dev(v_scratch, "v_scratch", torch.float32), _i32(status, "status"), _stream(stream)))
+
+
+def lora_sgmv_noalloc(y, x, pool, seg_offsets, seg_slot, layer, status=None, stream=None):
+    """lora_sgmv without a scratch argument, for callers that cannot allocate device memory; the
+    library's built-in scratch holds num_rows * r_max <= NOALLOC_MAX_FLOATS fp32 values and is
+    shared by all calls (order calls that could overlap on the GPU)."""
+    h = make_pool(pool)
+    _check(lib().lora_sgmv_noalloc(_dev(y, "y", h.dtype), _rows(y, "y", h.dtype), _dev(x, "x", h.dtype),
+                                   _rows(x, "x", h.dtype), h.ref, _i32(seg_offsets, "seg_offsets"),
+                                   _i32(seg_slot, "seg_slot"), int(seg_slot.numel()), int(y.shape[0]), int(layer),
+                                   _i32(status, "status"), _stream(stream)))
 
 
 def lora_bgmv(y, x, pool, row_slot, layer, v_scratch, status=None, stream=None):

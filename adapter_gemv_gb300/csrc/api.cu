@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <cstdio>
 #include <cstring>
 
@@ -194,6 +195,29 @@ mlora::ProblemDev problem(const mlora_pool *pool, int32_t layer, const void *x, 
   return q;
 }
 
+// Built-in scratch of lora_sgmv_noalloc: the v rows of one call (num_rows x r_max floats).
+// In host code the name is only a stand-in for the symbol; the device address comes from
+// cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) float g_noalloc_v[MLORA_NOALLOC_MAX_FLOATS];
+std::mutex g_noalloc_mu;
+float *g_noalloc_ptr[256] = {};  // device address per device ordinal
+
+int noalloc_scratch(float **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 256) return MLORA_ERR_SHAPE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_v);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch");
+    g_noalloc_ptr[dev] = static_cast<float *>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return MLORA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -261,6 +285,21 @@ int lora_sgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool
                   num_rows, dev_status, stream);
 }
 
+int lora_sgmv_noalloc(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool,
+                      const int32_t *seg_offsets, const int32_t *seg_slot, int32_t num_segments, int32_t num_rows,
+                      int32_t layer, int32_t *dev_status, void *stream) {
+  TRY(check_pool(pool, layer, true, true));
+  TRY(check_x(x, ldx, pool, num_rows));
+  TRY(check_y(y, ldy, pool, num_rows));
+  TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
+  if ((int64_t)num_rows * pool->r_max > MLORA_NOALLOC_MAX_FLOATS) return MLORA_ERR_TOO_LARGE;
+  if (num_rows == 0) return MLORA_OK;
+  float *v = nullptr;
+  TRY(noalloc_scratch(&v));
+  return run_sgmv(mlora::MODE_FUSED, pool, layer, x, ldx, y, ldy, v, seg_offsets, seg_slot, num_segments, num_rows,
+                  dev_status, stream);
+}
+
 int lora_bgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
               int32_t num_rows, int32_t layer, float *v_scratch, int32_t *dev_status, void *stream) {
   TRY(check_pool(pool, layer, true, true));
@@ -320,6 +359,7 @@ const char *lora_error_string(int code) {
     case MLORA_ERR_ALIGN: return "alignment rule broken (16-byte pointers, multiples of 8 elements)";
     case MLORA_ERR_POOL: return "malformed adapter pool descriptor";
     case MLORA_ERR_CUDA: return g_cuda_err;
+    case MLORA_ERR_TOO_LARGE: return "num_rows * r_max exceeds the built-in scratch (MLORA_NOALLOC_MAX_FLOATS)";
     default: return "unknown error code";
   }
 }

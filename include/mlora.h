@@ -92,6 +92,7 @@ extern "C" {
 #define MLORA_ERR_ALIGN (-4)       /* a pointer, leading dimension or size breaks the alignment rule */
 #define MLORA_ERR_POOL (-5)        /* malformed pool descriptor */
 #define MLORA_ERR_CUDA (-6)        /* a CUDA call failed; see lora_error_string(MLORA_ERR_CUDA) */
+#define MLORA_ERR_TOO_LARGE (-7)   /* the call needs more than the built-in scratch of lora_sgmv_noalloc */
 
 /* Device status bits, OR-ed into *dev_status. */
 #define MLORA_STATUS_BAD_OFFSETS 1
@@ -157,6 +158,30 @@ MLORA_API int lora_sgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const 
 
 MLORA_API int lora_bgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
               int32_t num_rows, int32_t layer, float *v_scratch, int32_t *dev_status, void *stream);
+
+/* ---- fused form without a scratch argument -------------------------------------------------
+ * lora_sgmv_noalloc: lora_sgmv for callers that cannot hand the library a device buffer --
+ * code that may not allocate device memory, such as a plugin running inside a host engine
+ * that owns all device memory and passes the plugin only its inputs and outputs, or a
+ * latency-critical path where cudaMalloc (which can synchronise the device) is not acceptable.
+ * Instead of v_scratch it uses an array built into the library: MLORA_NOALLOC_MAX_FLOATS fp32
+ * values (4 MiB) in device memory, which every GPU that loads the library holds until the
+ * process exits. The call itself allocates nothing (no cudaMalloc, no cudaFree, no library
+ * allocator).
+ *   - Limit: num_rows * pool->r_max <= MLORA_NOALLOC_MAX_FLOATS; a larger call returns
+ *     MLORA_ERR_TOO_LARGE and launches nothing.
+ *   - The first call on a device, with that device current, looks up the array's device
+ *     address (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call shares the one array, and it keeps the last call's contents. Nothing in it
+ *     must start at zero: the shrink writes every entry the expand later reads.
+ *   - Calls whose kernels may run at the same time on the GPU (other streams, other host
+ *     threads) race on the array; order them, e.g. on one stream.
+ * Same arguments, results and errors as lora_sgmv otherwise. (No counterpart on the pages:
+ * an interface convenience of this library.) */
+#define MLORA_NOALLOC_MAX_FLOATS (1 << 20)
+MLORA_API int lora_sgmv_noalloc(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool,
+                                const int32_t *seg_offsets, const int32_t *seg_slot, int32_t num_segments,
+                                int32_t num_rows, int32_t layer, int32_t *dev_status, void *stream);
 
 /* ---- grouped form: several projections over the same rows in one call --------------------
  * Punica builds the segments once per batch and reuses them for all 7 projections of every
