@@ -66,6 +66,23 @@ def dist_env():
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest `x` over all ranks (the job is as slow as its slowest replica); x itself when
+    there is no process group."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(world_size: int, rows_per_step: int, steps: int, slowest_secs: float) -> float:
+    """Whole-job throughput of `world_size` replicas: every rank processed rows_per_step rows per
+    step, the job took as long as its slowest rank."""
+    return world_size * rows_per_step * steps / slowest_secs
+
+
 class ClockSampler:
     """nvidia-smi clocks/throttle reasons sampled every 200 ms; keep the samples taken between
     start() and stop()."""
@@ -366,12 +383,9 @@ def run_ours(args):
     barrier()
     secs = time_graph(g, stream, args.steps, sampler)
     barrier()
-    if ws > 1:
-        t = torch.tensor([secs], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        secs = float(t.item())
+    secs = max_over_ranks(secs, dev)
     ms = secs / args.steps * 1e3
-    value = ws * rows * args.steps / secs
+    value = job_rows_per_s(ws, rows, args.steps, secs)
 
     # e2e: pinned host inputs -> device, the step, result back to the host, every step
     host_y = torch.empty(ybuf.shape, dtype=ybuf.dtype, pin_memory=True)
@@ -395,11 +409,7 @@ def run_ours(args):
             e2e_once()
         ev1.record(stream)
         ev1.synchronize()
-    e2e_secs = ev0.elapsed_time(ev1) / 1e3
-    if ws > 1:
-        t = torch.tensor([e2e_secs], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_secs = float(t.item())
+    e2e_secs = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, dev)
     h2d = ybuf.numel() * ybuf.element_size() + sum(x.numel() * x.element_size() for x in xs)
     d2h = ybuf.numel() * ybuf.element_size()
 
@@ -422,7 +432,7 @@ def run_ours(args):
                      "kernel": "decode_kernel<bf16, FUSED> (every launch of the step)",
                      "algorithmic_bytes_per_launch": bytes_step // plan.launches,
                      "traffic": ncu_traffic("decode_kernel_fused", "decode7b_distinct")},
-        "e2e": {"value": round(rows * e2e_steps / e2e_secs * ws, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(job_rows_per_s(ws, rows, e2e_steps, e2e_secs), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_secs / e2e_steps * 1e3, 4),
                 "api": "lora_sgmv_grouped via the Python binding, replayed as a CUDA graph; pinned host buffers"},
         "gpu_launches": plan.launches * args.steps,
@@ -443,32 +453,87 @@ def run_ours(args):
 
 
 def run_reference(args):
-    """The oracle as the reference arm: host cores, bounded sample per step, same metric."""
+    """The oracle as the reference arm: host cores, same metric and workload. Each step is a
+    bounded sample -- some rows of one layer's 7 projections -- scaled to the whole step
+    (32 rows x 224 ops), sized so that the whole --steps/--warmup run takes about
+    REFERENCE_BUDGET_S seconds."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    w = W.sgmv_decode_7b(device="cpu", dist="distinct", num_layers=2)  # per-layer work equals the full step's
+    w = W.sgmv_decode_7b(device="cpu", dist="distinct", num_layers=1)  # one layer: the step's per-layer work
     import oracle
     off, ss = w.batch.seg_offsets.numpy(), w.batch.seg_slot.numpy()
-    per_layer = {layer: _oracle_layer_inputs(w, layer) for layer in range(2)}
-    def one(layer):
+    inputs = _oracle_layer_inputs(w, 0)
+    M = w.batch.M
+
+    def one(rows):
         t0 = time.perf_counter()
-        for opool, x, y in per_layer[layer]:
-            oracle.sgmv(opool, 0, x, y, off, ss)
+        for opool, x, y in inputs:
+            oracle.sgmv(opool, 0, x, y, off, ss, rows=rows)
         return time.perf_counter() - t0
+
+    per_row = one([0])  # calibration: one row of the 7 ops
+    budget = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)
+    n = int(min(M, max(1, budget // max(per_row, 1e-9))))
     for k in range(args.warmup):
-        one(k % 2)
-    times = [one(k % 2) for k in range(args.steps)]
-    per_step = sum(times) / len(times) * 32
-    value = w.batch.M / per_step
-    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 3), "higher_is_better": True,
+        one([(k * n + i) % M for i in range(n)])
+    per_step = []
+    for k in range(args.steps):
+        t = one([(k * n + i) % M for i in range(n)])
+        per_step.append(t * (M / n) * 32)  # scale to all rows and all 32 layers
+    step_s = sum(per_step) / len(per_step)
+    value = M / step_s
+    sample = f"each step: the fp64 oracle on {n} of {M} rows of one layer's 7 projections, scaled x{M / n * 32:.0f}"
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": WORKLOAD},
-            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": "each step: the fp64 oracle on one layer (7 ops) of the step, x32"},
-            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+REFERENCE_BUDGET_S = 120.0
+
+
+NCU_TARGETS = ("decode7b", "decode7b-2layers", "q_proj", "prefill13b-q", "paged70b")
+
+
+def run_ncu_target(name: str, reps: int):
+    """Run one workload `reps` times with no timing, as a target for ncu (nothing is printed but
+    'ok'). decode7b-2layers is the decode step with 2 layers: the same launches per layer, a
+    smaller footprint for multi-pass captures."""
+    import adapter_gemv_gb300 as m
+    from adapter_gemv_gb300.plan import StepPlan
+    dev = torch.device("cuda", 0)
+    if name.startswith("decode7b"):
+        w = W.sgmv_decode_7b(device=dev, num_layers=2 if name.endswith("2layers") else 32)
+        plan = StepPlan(w.ops, w.batch)
+        for _ in range(reps):
+            plan()
+    elif name == "q_proj":
+        w = W.bgmv_decode_q(device=dev)
+        op = w.ops[0]
+        h = m.make_pool(op.pool)
+        v = torch.empty((w.batch.M, op.pool.r_max), dtype=torch.float32, device=dev)
+        for _ in range(reps):
+            m.lora_bgmv(op.y, op.x, h, w.batch.row_slot, 0, v)
+    elif name == "prefill13b-q":
+        w = W.sgmv_prefill_13b(device=dev, projections=W.LLAMA2_13B[:1])
+        op = w.ops[0]
+        h = m.make_pool(op.pool)
+        v = torch.empty((w.batch.M, op.pool.r_max), dtype=torch.float32, device=dev)
+        for _ in range(reps):
+            m.lora_sgmv(op.y, op.x, h, w.batch.seg_offsets, w.batch.seg_slot, 0, v)
+    elif name == "paged70b":
+        w = W.paged_decode_70b(device=dev)
+        op = w.ops[0]
+        h = m.make_pool(op.pool)
+        v = torch.empty((w.batch.M, op.pool.r_max), dtype=torch.float32, device=dev)
+        for _ in range(reps):
+            m.lora_bgmv(op.y, op.x, h, w.batch.row_slot, 0, v)
+    torch.cuda.synchronize()
+    print("ok", name)
 
 
 def main():
@@ -480,7 +545,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
+    ap.add_argument("--ncu-target", choices=NCU_TARGETS, help="run one workload untimed, as an ncu target")
+    ap.add_argument("--reps", type=int, default=2)
     args = ap.parse_args()
+    if args.ncu_target:
+        run_ncu_target(args.ncu_target, args.reps)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
