@@ -45,6 +45,15 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
   f[6] = Elem<DT>::lo(u.w); f[7] = Elem<DT>::hi(u.w);
 }
 
+// 8 packed 16-bit elements -> 4 float pairs, for the paired fp32 FMA (__ffma2_rn)
+template <int DT>
+__device__ __forceinline__ void unpack8x2(const uint4 &u, float2 (&f)[4]) {
+  f[0] = make_float2(Elem<DT>::lo(u.x), Elem<DT>::hi(u.x));
+  f[1] = make_float2(Elem<DT>::lo(u.y), Elem<DT>::hi(u.y));
+  f[2] = make_float2(Elem<DT>::lo(u.z), Elem<DT>::hi(u.z));
+  f[3] = make_float2(Elem<DT>::lo(u.w), Elem<DT>::hi(u.w));
+}
+
 template <int DT>
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   uint4 u;

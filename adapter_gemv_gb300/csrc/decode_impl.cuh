@@ -64,32 +64,66 @@ __device__ __forceinline__ const uint16_t *b_row(const PoolDev &pl, int s, int l
 // Resolve virtual tile `t` of problem `pr` into `ti` (whole block participates; reads only
 // metadata that no kernel of this library writes).
 // SGMV: segments contribute ceil(len / rt) tiles each, in segment order. BGMV: tile t is row t.
+// Every metadata load of the first scan round (offsets, slots, the pool's rank and scale tables
+// when it has at most RANK_CACHE slots) is in flight at once: one round trip to memory.
 template <int MODE>
 __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t, TileInfo *ti, int32_t *scan,
                              int32_t *rank_c, float *scale_c) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool cached = pr.pool.num_slots <= RANK_CACHE;
+  const bool sgmv = p.seg_off != nullptr;
+  const int cnt0 = sgmv ? min(SCAN_CAP, p.nseg) : 0;
+  constexpr int RC = RANK_CACHE / NTHREADS;
+  constexpr int SC = (SCAN_CAP + 1 + NTHREADS - 1) / NTHREADS;
+  int32_t rk[RC], so[SC], ss[SC];
+  float sc[RC];
+  int32_t row_slot = 0;
+#pragma unroll
+  for (int i = 0; i < RC; ++i) {
+    const int q = tid + i * NTHREADS;
+    if (cached && q < pr.pool.num_slots) {
+      rk[i] = pr.pool.rank[q];
+      sc[i] = pr.pool.scale[q];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < SC; ++i) {
+    const int q = tid + i * NTHREADS;
+    if (sgmv && q <= cnt0) so[i] = p.seg_off[q];
+    if (sgmv && q < cnt0) ss[i] = p.seg_slot[q];
+  }
+  if (!sgmv && tid == 0 && t < p.M) row_slot = p.row_slot[t];
+#pragma unroll
+  for (int i = 0; i < RC; ++i) {
+    const int q = tid + i * NTHREADS;
+    if (cached && q < pr.pool.num_slots) {
+      rank_c[q] = rk[i];
+      scale_c[q] = sc[i];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < SC; ++i) {
+    const int q = tid + i * NTHREADS;
+    if (sgmv && q <= cnt0) scan[q] = so[i];
+    if (sgmv && q < cnt0) scan[SCAN_CAP + 1 + q] = ss[i];
+  }
   if (tid == 0) {
     ti->skip = 1;
     ti->bad = 0;
     ti->nr = 0;
   }
-  if (cached) {  // loaded together with the row metadata: one round trip for the whole resolve
-    for (int q = tid; q < pr.pool.num_slots; q += NTHREADS) {
-      rank_c[q] = pr.pool.rank[q];
-      scale_c[q] = pr.pool.scale[q];
-    }
-  }
   __syncthreads();
-  if (p.seg_off != nullptr) {
+  if (sgmv) {
     int32_t carry = 0, found = 0, bad = 0;
     for (int base = 0; base < p.nseg; base += SCAN_CAP) {
       const int cnt = min(SCAN_CAP, p.nseg - base);
-      for (int q = tid; q <= cnt; q += NTHREADS) {
-        scan[q] = p.seg_off[base + q];
-        if (q < cnt) scan[SCAN_CAP + 1 + q] = p.seg_slot[base + q];  // one round trip for both
+      if (base > 0) {  // later rounds (more than SCAN_CAP segments): load, then scan
+        for (int q = tid; q <= cnt; q += NTHREADS) {
+          scan[q] = p.seg_off[base + q];
+          if (q < cnt) scan[SCAN_CAP + 1 + q] = p.seg_slot[base + q];
+        }
+        __syncthreads();
       }
-      __syncthreads();
       if (warp == 0) {
         if (lane == 0 && ((base == 0 && scan[0] != 0) || (base + cnt == p.nseg && scan[cnt] != p.M))) bad = 1;
         for (int q0 = 0; q0 < cnt; q0 += 32) {
@@ -120,86 +154,98 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
           carry += __shfl_sync(0xffffffffu, incl, 31);
         }
         bad = __any_sync(0xffffffffu, bad);
-        if (lane == 0) {
-          if (bad) {
-            ti->bad = MLORA_STATUS_BAD_OFFSETS;
-            found = 0;
-          }
+        if (lane == 0 && bad) {
+          ti->bad = MLORA_STATUS_BAD_OFFSETS;
+          found = 0;
         }
       }
       if (base + SCAN_CAP < p.nseg) __syncthreads();  // the next round overwrites scan
     }
-    if (p.nseg == 0 && tid == 0 && p.seg_off[0] != p.M) ti->bad = MLORA_STATUS_BAD_OFFSETS;
+    if (p.nseg == 0 && tid == 0 && scan[0] != p.M) ti->bad = MLORA_STATUS_BAD_OFFSETS;
     if (tid == 0) ti->skip = (found && !ti->bad) ? 0 : 1;
   } else if (tid == 0 && t < p.M) {
     ti->row0 = t;
     ti->nr = 1;
-    ti->slot = p.row_slot[t];
+    ti->slot = row_slot;
     ti->skip = 0;
-  }  // (the BGMV slot load overlaps the rank/scale table loads above: both precede one barrier)
-  __syncthreads();
-  // Adapter checks (warp 0): slot range, rank range, page ids of the rank-rows this mode reads.
-  if (warp == 0 && !ti->skip) {
-    const int s = ti->slot;
-    const PoolDev &pl = pr.pool;
-    int32_t bad = 0, skip = 0, rank = 0;
-    float scale = 0.f;
-    if (s == -1) {
-      skip = 1;
-    } else if (s < -1 || s >= pl.num_slots) {
-      bad = MLORA_STATUS_BAD_SLOT;
-    } else {
-      rank = cached ? rank_c[s] : pl.rank[s];
-      scale = cached ? scale_c[s] : pl.scale[s];
-      if (rank < 1 || rank > pl.r_max) {
-        bad = MLORA_STATUS_BAD_RANK;
-      } else if (pl.kind == MLORA_POOL_PAGED) {
-        const int64_t t0 = ((int64_t)s * pl.num_layers + pr.layer) * pl.r_max;
-        int32_t badp = 0;
-        for (int j = lane; j < rank; j += 32) {
-          if (MODE != MODE_EXPAND) {
-            const int32_t pg = pl.a_tab[t0 + j];
-            badp |= (pg < 0 || pg >= pl.num_pages);
+  }
+  // Adapter checks (warp 0, which wrote the tile above): slot range, rank range, page ids of
+  // the rank-rows this mode reads.
+  if (warp == 0) {
+    __syncwarp();
+    if (!ti->skip) {
+      const int s = ti->slot;
+      const PoolDev &pl = pr.pool;
+      int32_t bad = 0, skip = 0, rank = 0;
+      float scale = 0.f;
+      if (s == -1) {
+        skip = 1;
+      } else if (s < -1 || s >= pl.num_slots) {
+        bad = MLORA_STATUS_BAD_SLOT;
+      } else {
+        rank = cached ? rank_c[s] : pl.rank[s];
+        scale = cached ? scale_c[s] : pl.scale[s];
+        if (rank < 1 || rank > pl.r_max) {
+          bad = MLORA_STATUS_BAD_RANK;
+        } else if (pl.kind == MLORA_POOL_PAGED) {
+          const int64_t t0 = ((int64_t)s * pl.num_layers + pr.layer) * pl.r_max;
+          int32_t badp = 0;
+          for (int j = lane; j < rank; j += 32) {
+            if (MODE != MODE_EXPAND) {
+              const int32_t pg = pl.a_tab[t0 + j];
+              badp |= (pg < 0 || pg >= pl.num_pages);
+            }
+            if (MODE != MODE_SHRINK) {
+              const int32_t pg = pl.b_tab[t0 + j];
+              badp |= (pg < 0 || pg >= pl.num_pages);
+            }
           }
-          if (MODE != MODE_SHRINK) {
-            const int32_t pg = pl.b_tab[t0 + j];
-            badp |= (pg < 0 || pg >= pl.num_pages);
-          }
+          if (__any_sync(0xffffffffu, badp)) bad = MLORA_STATUS_BAD_PAGE;
         }
-        if (__any_sync(0xffffffffu, badp)) bad = MLORA_STATUS_BAD_PAGE;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        ti->rank = rank;
+        ti->scale = scale;
+        ti->bad |= bad;
+        ti->skip = (skip || bad) ? 1 : 0;
       }
     }
-    if (lane == 0) {
-      ti->rank = rank;
-      ti->scale = scale;
-      ti->bad |= bad;
-      ti->skip = (skip || bad) ? 1 : 0;
-    }
   }
+  // The scan and table area is reused for staged B rows, written by bulk copies (the async
+  // proxy): order this thread's accesses to it before them.
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
 }
 
 // Shared-memory layout (dynamic):
-//   [0, 64)      mbarriers: xbar (exchange), bbar (B rows staged in shared memory)
+//   [0, 64)      mbarriers: xbar (exchange), bbar (B rows staged), ibar (x slice), ybar (y slice)
 //   [64, 96)     TileInfo
 //   gbuf         [cs][RT][r_alloc] floats: every CTA's partial v (cluster modes)
 //   vsm          [RT][r_alloc] floats: the summed v of the tile
-//   scan         [2 * SCAN_CAP + 1] ints: segment offsets and slots while resolving the tile
-//   rank_c/scale_c [RANK_CACHE] ints / floats: the pool's rank and scale tables (small pools)
 //   xs           [RT][kb] elements: one pass of the tile's x rows (shrink)
-//   bs           [r_alloc][nb] elements: this CTA's B rows, when staged (expand)
+//   ys           [ny] elements: the y slice of a one-row tile, when staged (expand)
+//   then one region used twice:
+//     while resolving the tile: scan [2 * SCAN_CAP + 1] ints (segment offsets and slots) and
+//                               rank_c / scale_c [RANK_CACHE] (the pool's rank and scale tables)
+//     afterwards:               bs [r_alloc][nb] elements, this CTA's B rows when staged
+//   Sharing the region keeps a CTA that stages B small enough to sit on an SM beside a CTA of
+//   the neighbouring launch.
 struct Layout {
-  int gbuf, vsm, scan, rank_c, scale_c, xs, bs, total;
-  __host__ __device__ static Layout make(int cs, int rt, int r_alloc, int kb, int nb_staged) {
+  int gbuf, vsm, xs, ys, scan, rank_c, scale_c, bs, total;
+  __host__ __device__ static Layout make(int cs, int rt, int r_alloc, int kb, int nb_staged, int ny) {
     Layout L;
     L.gbuf = 128;
     L.vsm = L.gbuf + cs * rt * r_alloc * 4;
-    L.scan = L.vsm + rt * r_alloc * 4;
+    L.xs = (L.vsm + rt * r_alloc * 4 + 127) & ~127;
+    L.ys = (L.xs + rt * kb * 2 + 127) & ~127;
+    L.scan = (L.ys + ny * 2 + 127) & ~127;
     L.rank_c = L.scan + (2 * SCAN_CAP + 1) * 4;
     L.scale_c = L.rank_c + RANK_CACHE * 4;
-    L.xs = (L.scale_c + RANK_CACHE * 4 + 127) & ~127;
-    L.bs = (L.xs + rt * kb * 2 + 127) & ~127;
-    L.total = L.bs + r_alloc * nb_staged * 2;
+    const int resolve_end = L.scale_c + RANK_CACHE * 4;
+    L.bs = L.scan;
+    const int staged_end = L.bs + r_alloc * nb_staged * 2;
+    L.total = resolve_end > staged_end ? resolve_end : staged_end;
     return L;
   }
 };
@@ -220,9 +266,11 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   constexpr int KB = Pass<JPW>::KB;
   const int cs = p.csplit;  // CTAs per tile: the cluster (SHRINK, FUSED) or the N-split (EXPAND)
   const bool stage_b = p.nb > 0;  // B rows of the CTA's slice go to shared memory before the wait
-  const Layout L = Layout::make(MODE == MODE_EXPAND ? 1 : cs, RT, p.r_alloc, KB, p.nb);
+  const Layout L = Layout::make(MODE == MODE_EXPAND ? 1 : cs, RT, p.r_alloc, KB, p.nb, p.ny);
   uint64_t *xbar = reinterpret_cast<uint64_t *>(smem);
   uint64_t *bbar = xbar + 1;
+  uint64_t *ibar = xbar + 2;
+  uint64_t *ybar = xbar + 3;
   TileInfo *ti = reinterpret_cast<TileInfo *>(smem + 64);
   float *gbuf = reinterpret_cast<float *>(smem + L.gbuf);
   float *vsm = reinterpret_cast<float *>(smem + L.vsm);
@@ -230,6 +278,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   int32_t *rank_c = reinterpret_cast<int32_t *>(smem + L.rank_c);
   float *scale_c = reinterpret_cast<float *>(smem + L.scale_c);
   uint16_t *xs = reinterpret_cast<uint16_t *>(smem + L.xs);
+  uint16_t *ys = reinterpret_cast<uint16_t *>(smem + L.ys);
   uint16_t *bs = reinterpret_cast<uint16_t *>(smem + L.bs);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -244,6 +293,8 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   if (tid == 0) {
     mbar_init(xbar, 1);
     mbar_init(bbar, 1);
+    mbar_init(ibar, 1);
+    mbar_init(ybar, 1);
     mbar_fence_init();
   }
   __syncthreads();
@@ -264,6 +315,10 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   const bool do_shrink = MODE != MODE_EXPAND && active;
   const bool do_expand = MODE != MODE_SHRINK && active;
   const bool b_staged = do_expand && stage_b && n_end > n_begin;
+  // One-row tiles whose d_in slice is a single pass take their x slice (and, when the launcher
+  // made room, their y slice) into shared memory by bulk copies issued right after the wait.
+  const bool x_bulk = RT == 1 && do_shrink && k_end > k_begin && k_end - k_begin <= KB;
+  const bool y_bulk = RT == 1 && do_expand && p.ny > 0 && n_end > n_begin;
   const uint64_t evict_first = policy_evict_first();
 
   // Everything that no kernel writes -- the adapter rows -- is requested before waiting for the
@@ -329,23 +384,28 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
 #pragma unroll
       for (int u = 0; u < UK; ++u) {
         const int c8 = lane + 32 * u;
-        if (j < rank && c8 < n8) a[jj][u] = ldg_stream(a_row(pl, s, pr.layer, j) + kb0 + c8 * 8, evict_first);
+        // zero outside the slice and the rank: the one-row loop below then needs no guards
+        a[jj][u] = (j < rank && c8 < n8) ? ldg_stream(a_row(pl, s, pr.layer, j) + kb0 + c8 * 8, evict_first)
+                                         : make_uint4(0u, 0u, 0u, 0u);
       }
     }
   };
   if (do_shrink) load_a(k_begin);
+  if (x_bulk)  // the bulk copy fills xs up to the slice end; zeros beyond it (disjoint bytes)
+    for (int c8 = ((k_end - k_begin) >> 3) + tid; c8 < KB / 8; c8 += NTHREADS)
+      *reinterpret_cast<uint4 *>(xs + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
 
   pdl_wait();  // the previous kernel in the stream has finished; its writes are visible
 
-  // y of this thread's first YPRE column chunks (one-row tiles), requested now so it is here by
-  // the expand
-  constexpr int YPRE = 4;
-  uint4 ypre[YPRE];
-  if (RT == 1 && do_expand) {
-    const int n8 = (n_end - n_begin) >> 3;
-#pragma unroll
-    for (int q = 0; q < YPRE; ++q)
-      if (tid + q * NTHREADS < n8) ypre[q] = ldg_u4(pr.y + (int64_t)row0 * pr.ldy + n_begin + (tid + q * NTHREADS) * 8);
+  if (tid == 0) {
+    if (x_bulk) {
+      mbar_arrive_expect_tx(ibar, (uint32_t)(k_end - k_begin) * 2);
+      bulk_g2s(xs, pr.x + (int64_t)row0 * pr.ldx + k_begin, (uint32_t)(k_end - k_begin) * 2, ibar);
+    }
+    if (y_bulk) {
+      mbar_arrive_expect_tx(ybar, (uint32_t)(n_end - n_begin) * 2);
+      bulk_g2s(ys, pr.y + (int64_t)row0 * pr.ldy + n_begin, (uint32_t)(n_end - n_begin) * 2, ybar);
+    }
   }
   int timed_out = 0;
 
@@ -357,7 +417,42 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
 #pragma unroll
       for (int jj = 0; jj < JPW; ++jj) acc[i][jj] = 0.f;
 
-    if (do_shrink) {
+    if (x_bulk) {
+      // One row, one pass: each lane reads its x chunks from shared memory, unpacks each once
+      // for all its rank rows and accumulates pairs of products with the paired fp32 FMA (two
+      // independent chains per rank row when a warp has at most 2 rank rows).
+      const int ok = mbar_wait(ibar, 0) ? 1 : 0;
+      timed_out = __syncthreads_or(!ok);
+      if (!timed_out) {
+        // No guards: A is zero outside the slice and the rank, x is zero past the slice, so
+        // every chunk and rank row of the pass runs unconditionally (straight-line code).
+        constexpr int CH = JPW <= 2 ? 2 : 1;
+        float2 acc2[JPW][CH];
+#pragma unroll
+        for (int jj = 0; jj < JPW; ++jj)
+#pragma unroll
+          for (int h = 0; h < CH; ++h) acc2[jj][h] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < UK; ++u) {
+          float2 x2[4];
+          unpack8x2<DT>(*reinterpret_cast<const uint4 *>(xs + (lane + 32 * u) * 8), x2);
+#pragma unroll
+          for (int jj = 0; jj < JPW; ++jj) {
+            float2 a2[4];
+            unpack8x2<DT>(a[jj][u], a2);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc2[jj][e % CH] = __ffma2_rn(x2[e], a2[e], acc2[jj][e % CH]);
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < JPW; ++jj) {
+          float2 t2 = acc2[jj][0];
+#pragma unroll
+          for (int h = 1; h < CH; ++h) t2 = make_float2(t2.x + acc2[jj][h].x, t2.y + acc2[jj][h].y);
+          acc[0][jj] = t2.x + t2.y;
+        }
+      }
+    } else if (do_shrink) {
       for (int kb0 = k_begin; kb0 < k_end; kb0 += KB) {
         const int n8 = min(KB, k_end - kb0) >> 3;
         if (kb0 != k_begin) load_a(kb0);
@@ -408,8 +503,9 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
 
     if (clustered) {
       // Push this CTA's partials into slot c of every peer's gather buffer (lane q -> CTA q).
+      // A CTA that timed out pushes nothing; its peers then time out too and skip the tile.
       cluster_wait();  // every peer has initialised its exchange barrier
-      if (do_shrink && lane < cs) {
+      if (do_shrink && !timed_out && lane < cs) {
         const uint32_t peer_gbuf = dsmem_addr(gbuf, lane);
         const uint32_t peer_bar = dsmem_addr(xbar, lane);
 #pragma unroll
@@ -425,7 +521,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       }
       if (do_shrink) {
         const int ok = mbar_wait_cluster(xbar, 0) ? 1 : 0;
-        timed_out = __syncthreads_or(!ok);
+        timed_out |= __syncthreads_or(!ok);
         if (!timed_out) {
           for (int e = tid; e < nr * rank; e += NTHREADS) {
             const int i = e / rank, j = e % rank;
@@ -439,7 +535,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
           }
         }
       }
-    } else if (do_shrink && lane == 0) {
+    } else if (do_shrink && !timed_out && lane == 0) {
 #pragma unroll
       for (int jj = 0; jj < JPW; ++jj) {
         const int j = warp + jj * NWARPS;
@@ -454,91 +550,164 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
         }
       }
     }
-    __syncthreads();
   } else if (active) {
     // expand only: this tile's v rows from global memory (written by the previous kernel)
     for (int e = tid; e < nr * rank; e += NTHREADS) {
       const int i = e / rank, j = e % rank;
       vsm[i * p.r_alloc + j] = pr.v[(int64_t)(row0 + i) * pl.r_max + j];
     }
-    __syncthreads();
+  }
+  // v is published to every thread by this barrier, which also agrees on the staged B rows and
+  // the staged y slice having landed.
+  {
+    int ok = 1;
+    if (b_staged && !timed_out) ok &= mbar_wait(bbar, 0) ? 1 : 0;
+    if (y_bulk && !timed_out) ok &= mbar_wait(ybar, 0) ? 1 : 0;
+    timed_out |= __syncthreads_or(!ok);
   }
 
   // ---------------- expand: y[rows][this CTA's slice of d_out] ----------------
-  if (b_staged && !timed_out) {
-    const int ok = mbar_wait(bbar, 0) ? 1 : 0;
-    timed_out = __syncthreads_or(!ok);
-  }
   if (do_expand && !timed_out) {
     const int n8 = (n_end - n_begin) >> 3;
-    for (int c8 = tid; c8 < n8; c8 += NTHREADS) {
-      const int n0 = n_begin + c8 * 8;
-      float acc[RT][8];
+    if (RT == 1) {
+      // One row: 8 columns per thread and pass, rank rows summed with the paired fp32 FMA in
+      // two chains (even and odd rank rows); v sits in registers for ranks up to 16.
+      constexpr bool VREG = JPW <= 2;
+      constexpr int RV = VREG ? 8 * JPW : 1;
+      float vr[RV];
 #pragma unroll
-      for (int i = 0; i < RT; ++i)
+      for (int j = 0; j < RV; ++j) vr[j] = (VREG && j < rank) ? vsm[j] : 0.f;
+      for (int c8 = tid; c8 < n8; c8 += NTHREADS) {
+        const int n0 = n_begin + c8 * 8;
+        float2 ev[4], od[4];  // even / odd rank rows
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
-      if (b_staged) {
-        for (int j = 0; j < rank; ++j) {
-          float bf[8];
-          unpack8<DT>(*reinterpret_cast<const uint4 *>(bs + j * p.nb + c8 * 8), bf);
+        for (int e = 0; e < 4; ++e) ev[e] = od[e] = make_float2(0.f, 0.f);
+        auto add_row = [&](const uint4 &bw, float vj, float2 (&acc2)[4]) {
+          float2 b2[4];
+          unpack8x2<DT>(bw, b2);
+          const float2 v2 = make_float2(vj, vj);
 #pragma unroll
-          for (int i = 0; i < RT; ++i) {
-            if (i < nr) {
-              const float vij = vsm[i * p.r_alloc + j];
+          for (int e = 0; e < 4; ++e) acc2[e] = __ffma2_rn(v2, b2[e], acc2[e]);
+        };
+        constexpr int UB = 8;  // B rows in flight per thread when they come from global memory
+        if constexpr (VREG) {
+          if (b_staged) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(vij, bf[e], acc[i][e]);
+            for (int j = 0; j < RV; j += 2) {
+              if (j < rank) add_row(*reinterpret_cast<const uint4 *>(bs + j * p.nb + c8 * 8), vr[j], ev);
+              if (j + 1 < rank) add_row(*reinterpret_cast<const uint4 *>(bs + (j + 1) * p.nb + c8 * 8), vr[j + 1], od);
+            }
+          } else {
+#pragma unroll
+            for (int j0 = 0; j0 < RV; j0 += UB) {
+              uint4 bq[UB];
+#pragma unroll
+              for (int u = 0; u < UB; ++u)
+                if (j0 + u < rank) bq[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+#pragma unroll
+              for (int u = 0; u < UB; u += 2) {
+                if (j0 + u < rank) add_row(bq[u], vr[j0 + u], ev);
+                if (j0 + u + 1 < rank) add_row(bq[u + 1], vr[j0 + u + 1], od);
+              }
+            }
+          }
+        } else {
+          if (b_staged) {
+#pragma unroll 2
+            for (int j = 0; j < rank; j += 2) {
+              add_row(*reinterpret_cast<const uint4 *>(bs + j * p.nb + c8 * 8), vsm[j], ev);
+              if (j + 1 < rank) add_row(*reinterpret_cast<const uint4 *>(bs + (j + 1) * p.nb + c8 * 8), vsm[j + 1], od);
+            }
+          } else {
+            for (int j0 = 0; j0 < rank; j0 += UB) {
+              uint4 bq[UB];
+#pragma unroll
+              for (int u = 0; u < UB; ++u)
+                if (j0 + u < rank) bq[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+#pragma unroll
+              for (int u = 0; u < UB; u += 2) {
+                if (j0 + u < rank) add_row(bq[u], vsm[j0 + u], ev);
+                if (j0 + u + 1 < rank) add_row(bq[u + 1], vsm[j0 + u + 1], od);
+              }
             }
           }
         }
-      } else {
-        constexpr int UB = RT == 1 ? 16 : 4;  // B loads in flight per thread
-        for (int j0 = 0; j0 < rank; j0 += UB) {
-          uint4 b[UB];
+        const uint4 yw = y_bulk ? *reinterpret_cast<const uint4 *>(ys + c8 * 8) : ldg_u4(pr.y + (int64_t)row0 * pr.ldy + n0);
+        float yf[8];
+        unpack8<DT>(yw, yf);
 #pragma unroll
-          for (int u = 0; u < UB; ++u)
-            if (j0 + u < rank) b[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+        for (int e = 0; e < 4; ++e) {
+          yf[2 * e] = fmaf(scale, ev[e].x + od[e].x, yf[2 * e]);
+          yf[2 * e + 1] = fmaf(scale, ev[e].y + od[e].y, yf[2 * e + 1]);
+        }
+        *reinterpret_cast<uint4 *>(pr.y + (int64_t)row0 * pr.ldy + n0) = pack8<DT>(yf);
+      }
+    } else {
+      for (int c8 = tid; c8 < n8; c8 += NTHREADS) {
+        const int n0 = n_begin + c8 * 8;
+        float acc[RT][8];
 #pragma unroll
-          for (int u = 0; u < UB; ++u) {
-            if (j0 + u < rank) {
-              float bf[8];
-              unpack8<DT>(b[u], bf);
+        for (int i = 0; i < RT; ++i)
 #pragma unroll
-              for (int i = 0; i < RT; ++i) {
-                if (i < nr) {
-                  const float vij = vsm[i * p.r_alloc + j0 + u];
+          for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+        if (b_staged) {
+          for (int j = 0; j < rank; ++j) {
+            float bf[8];
+            unpack8<DT>(*reinterpret_cast<const uint4 *>(bs + j * p.nb + c8 * 8), bf);
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(vij, bf[e], acc[i][e]);
+            for (int i = 0; i < RT; ++i) {
+              if (i < nr) {
+                const float vij = vsm[i * p.r_alloc + j];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(vij, bf[e], acc[i][e]);
+              }
+            }
+          }
+        } else {
+          constexpr int UB = 4;  // B loads in flight per thread
+          for (int j0 = 0; j0 < rank; j0 += UB) {
+            uint4 b[UB];
+#pragma unroll
+            for (int u = 0; u < UB; ++u)
+              if (j0 + u < rank) b[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+#pragma unroll
+            for (int u = 0; u < UB; ++u) {
+              if (j0 + u < rank) {
+                float bf[8];
+                unpack8<DT>(b[u], bf);
+#pragma unroll
+                for (int i = 0; i < RT; ++i) {
+                  if (i < nr) {
+                    const float vij = vsm[i * p.r_alloc + j0 + u];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(vij, bf[e], acc[i][e]);
+                  }
                 }
               }
             }
           }
         }
-      }
 #pragma unroll
-      for (int i = 0; i < RT; ++i) {
-        if (i < nr) {
-          float yf[8];
-          const int q = (c8 - tid) / NTHREADS;
-          uint4 yw;
-          if (RT == 1 && q < YPRE) {
+        for (int i = 0; i < RT; ++i) {
+          if (i < nr) {
+            float yf[8];
+            unpack8<DT>(ldg_u4(pr.y + (int64_t)(row0 + i) * pr.ldy + n0), yf);
 #pragma unroll
-            for (int qq = 0; qq < YPRE; ++qq)
-              if (qq == q) yw = ypre[qq];
-          } else {
-            yw = ldg_u4(pr.y + (int64_t)(row0 + i) * pr.ldy + n0);
+            for (int e = 0; e < 8; ++e) yf[e] = fmaf(scale, acc[i][e], yf[e]);
+            *reinterpret_cast<uint4 *>(pr.y + (int64_t)(row0 + i) * pr.ldy + n0) = pack8<DT>(yf);
           }
-          unpack8<DT>(yw, yf);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) yf[e] = fmaf(scale, acc[i][e], yf[e]);
-          *reinterpret_cast<uint4 *>(pr.y + (int64_t)(row0 + i) * pr.ldy + n0) = pack8<DT>(yf);
         }
       }
     }
   }
 
-  if (b_staged && timed_out) (void)mbar_wait(bbar, 0, 100000000ull);  // copies in flight land before exit
-  if (timed_out && tid == 0) report(p.status, MLORA_STATUS_TIMEOUT);
+  // Copies still in flight after a time-out land before the CTA exits (bounded waits).
+  if (timed_out) {
+    if (b_staged) (void)mbar_wait(bbar, 0, 100000000ull);
+    if (x_bulk) (void)mbar_wait(ibar, 0, 100000000ull);
+    if (y_bulk) (void)mbar_wait(ybar, 0, 100000000ull);
+    if (tid == 0) report(p.status, MLORA_STATUS_TIMEOUT);
+  }
   if (clustered) cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
 }
 

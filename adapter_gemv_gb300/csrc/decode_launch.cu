@@ -56,6 +56,7 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   // at least 256 elements of the split dimension per CTA; at most 16 per cluster.
   const int sms = sm_count();
   const int b_cap = 176 * 1024;
+  const int y_cap = 16 * 1024, y_total_cap = 96 * 1024;
   int cs_min = 1;
   if (mode != MODE_EXPAND) cs_min = (d_in_max + kb - 1) / kb;
   if (mode != MODE_SHRINK) {
@@ -76,8 +77,15 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   const int nchunk = ((d_out_max + cs - 1) / cs + 7) & ~7;
   p.nb = (mode != MODE_SHRINK && (int64_t)r_alloc * nchunk * 2 <= b_cap) ? nchunk : 0;
   p.kb = kb;
-  p.sk = p.se = 0;
-  const Layout L = Layout::make((mode == MODE_EXPAND) ? 1 : cs, p.rt, r_alloc, kb, p.nb);
+  p.spare = 0;
+  // One-row tiles also take their y slice into shared memory, if the CTA stays small enough
+  // to share an SM with another.
+  const int lcs = (mode == MODE_EXPAND) ? 1 : cs;
+  p.ny = 0;
+  if (p.rt == 1 && mode != MODE_SHRINK && nchunk * 2 <= y_cap &&
+      Layout::make(lcs, p.rt, r_alloc, kb, p.nb, nchunk).total <= y_total_cap)
+    p.ny = nchunk;
+  const Layout L = Layout::make(lcs, p.rt, r_alloc, kb, p.nb, p.ny);
   if (L.total > 227 * 1024) return cudaErrorInvalidConfiguration;
 
   const int64_t grid = units * cs;

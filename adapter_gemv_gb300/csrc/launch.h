@@ -43,7 +43,7 @@ struct DecodeParams {
   int32_t tc_min;  // > 0: segments of at least tc_min rows are done by the tensor-core kernels;
                    // these kernels take only the shorter segments
   // chosen by the launcher
-  int32_t rt, tiles, csplit, kb, nb, sk, se, r_alloc;
+  int32_t rt, tiles, csplit, kb, nb, ny, spare, r_alloc;  // nb: staged B columns; ny: y slice staged
 };
 
 // Tensor-core path for the full 128-row blocks of long SGMV segments (prefill_tc.cu).
