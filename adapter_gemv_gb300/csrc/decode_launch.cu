@@ -50,20 +50,22 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   // Rank rows per warp -> K elements per pass of A loads into registers.
   const int jpw = r_alloc <= 16 ? 2 : r_alloc <= 32 ? 4 : r_alloc <= 64 ? 8 : 16;
   const int kb = 256 * (16 / jpw);
-  // CTAs per tile (cs). Lower bounds: the CTA's slice of d_in is one pass of A loads, and its
-  // slice of B fits in shared memory (up to 176 KB). Otherwise about one CTA per SM for the
-  // launch, so most CTAs of the next launch (programmatic dependent launch) find room early;
-  // at least 256 elements of the split dimension per CTA; at most 16 per cluster.
+  // CTAs per tile (cs): the smallest split whose CTA slice of d_in is one pass of A loads and
+  // whose slice of B fits in 88 KB of shared memory (so two CTAs fit on an SM), raised until
+  // the launch has at least half as many CTAs as there are SMs; at least 256 elements of the
+  // split dimension per CTA; at most 16 per cluster. Fewer, fuller CTAs leave SM room for the
+  // next launch's CTAs (programmatic dependent launch) to start and fetch their adapter rows
+  // while this one runs.
   const int sms = sm_count();
-  const int b_cap = 176 * 1024;
-  const int y_cap = 16 * 1024, y_total_cap = 96 * 1024;
+  const int b_cap = 88 * 1024;
+  const int y_cap = 16 * 1024, y_total_cap = 110 * 1024;
   int cs_min = 1;
   if (mode != MODE_EXPAND) cs_min = (d_in_max + kb - 1) / kb;
   if (mode != MODE_SHRINK) {
     const int need = (int)(((int64_t)r_alloc * d_out_max * 2 + b_cap - 1) / b_cap);
     cs_min = cs_min > need ? cs_min : need;
   }
-  int cs = (int)(sms / units);
+  int cs = (int)((sms / 2 + units - 1) / units);
   cs = cs > cs_min ? cs : cs_min;
   const int split_dim = (mode == MODE_EXPAND) ? d_out_max : d_in_max;
   const int max_cs = split_dim / 256 > 1 ? split_dim / 256 : 1;
