@@ -224,7 +224,7 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
 //   gbuf         [cs][RT][r_alloc] floats: every CTA's partial v (cluster modes)
 //   vsm          [RT][r_alloc] floats: the summed v of the tile
 //   xs           [RT][kb] elements: one pass of the tile's x rows (shrink)
-//   ys           [ny] elements: the y slice of a one-row tile, when staged (expand)
+//   ys           [RT][ny] elements: the y rows' slices, when staged (expand)
 //   then one region used twice:
 //     while resolving the tile: scan [2 * SCAN_CAP + 1] ints (segment offsets and slots) and
 //                               rank_c / scale_c [RANK_CACHE] (the pool's rank and scale tables)
@@ -239,7 +239,7 @@ struct Layout {
     L.vsm = L.gbuf + cs * rt * r_alloc * 4;
     L.xs = (L.vsm + rt * r_alloc * 4 + 127) & ~127;
     L.ys = (L.xs + rt * kb * 2 + 127) & ~127;
-    L.scan = (L.ys + ny * 2 + 127) & ~127;
+    L.scan = (L.ys + rt * ny * 2 + 127) & ~127;
     L.rank_c = L.scan + (2 * SCAN_CAP + 1) * 4;
     L.scale_c = L.rank_c + RANK_CACHE * 4;
     const int resolve_end = L.scale_c + RANK_CACHE * 4;
@@ -315,10 +315,10 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   const bool do_shrink = MODE != MODE_EXPAND && active;
   const bool do_expand = MODE != MODE_SHRINK && active;
   const bool b_staged = do_expand && stage_b && n_end > n_begin;
-  // One-row tiles whose d_in slice is a single pass take their x slice (and, when the launcher
-  // made room, their y slice) into shared memory by bulk copies issued right after the wait.
-  const bool x_bulk = RT == 1 && do_shrink && k_end > k_begin && k_end - k_begin <= KB;
-  const bool y_bulk = RT == 1 && do_expand && p.ny > 0 && n_end > n_begin;
+  // Tiles whose d_in slice is a single pass take their x rows (and, when the launcher made
+  // room, their y rows) into shared memory by bulk copies issued right after the wait.
+  const bool x_bulk = do_shrink && k_end > k_begin && k_end - k_begin <= KB;
+  const bool y_bulk = do_expand && p.ny > 0 && n_end > n_begin;
   const uint64_t evict_first = policy_evict_first();
 
   // Everything that no kernel writes -- the adapter rows -- is requested before waiting for the
@@ -391,20 +391,26 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
     }
   };
   if (do_shrink) load_a(k_begin);
-  if (x_bulk)  // the bulk copy fills xs up to the slice end; zeros beyond it (disjoint bytes)
-    for (int c8 = ((k_end - k_begin) >> 3) + tid; c8 < KB / 8; c8 += NTHREADS)
-      *reinterpret_cast<uint4 *>(xs + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
+  if (x_bulk) {  // the bulk copies fill xs rows < nr up to the slice end; zeros elsewhere (disjoint bytes)
+    const int s8 = (k_end - k_begin) >> 3;
+    for (int e = tid; e < RT * (KB / 8); e += NTHREADS) {
+      const int i = e / (KB / 8), c8 = e % (KB / 8);
+      if (i >= nr || c8 >= s8) *reinterpret_cast<uint4 *>(xs + i * KB + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
 
   pdl_wait();  // the previous kernel in the stream has finished; its writes are visible
 
   if (tid == 0) {
     if (x_bulk) {
-      mbar_arrive_expect_tx(ibar, (uint32_t)(k_end - k_begin) * 2);
-      bulk_g2s(xs, pr.x + (int64_t)row0 * pr.ldx + k_begin, (uint32_t)(k_end - k_begin) * 2, ibar);
+      mbar_arrive_expect_tx(ibar, (uint32_t)(nr * (k_end - k_begin) * 2));
+      for (int i = 0; i < nr; ++i)
+        bulk_g2s(xs + i * KB, pr.x + (int64_t)(row0 + i) * pr.ldx + k_begin, (uint32_t)(k_end - k_begin) * 2, ibar);
     }
     if (y_bulk) {
-      mbar_arrive_expect_tx(ybar, (uint32_t)(n_end - n_begin) * 2);
-      bulk_g2s(ys, pr.y + (int64_t)row0 * pr.ldy + n_begin, (uint32_t)(n_end - n_begin) * 2, ybar);
+      mbar_arrive_expect_tx(ybar, (uint32_t)(nr * (n_end - n_begin) * 2));
+      for (int i = 0; i < nr; ++i)
+        bulk_g2s(ys + i * p.ny, pr.y + (int64_t)(row0 + i) * pr.ldy + n_begin, (uint32_t)(n_end - n_begin) * 2, ybar);
     }
   }
   int timed_out = 0;
@@ -423,7 +429,33 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       // independent chains per rank row when a warp has at most 2 rank rows).
       const int ok = mbar_wait(ibar, 0) ? 1 : 0;
       timed_out = __syncthreads_or(!ok);
-      if (!timed_out) {
+      if (!timed_out && RT > 1) {
+        // Several rows: A is unpacked once per chunk for a pair of rank rows, then every row's x
+        // chunk meets both; no guards (A is zero outside the slice and the rank, x is zero in
+        // rows past nr and past the slice).
+        constexpr int JG = JPW < 2 ? JPW : 2;
+#pragma unroll
+        for (int jg = 0; jg < JPW; jg += JG) {
+#pragma unroll
+          for (int u = 0; u < UK; ++u) {
+            float af[JG][8];
+#pragma unroll
+            for (int q = 0; q < JG; ++q) unpack8<DT>(a[jg + q][u], af[q]);
+#pragma unroll
+            for (int i = 0; i < RT; ++i) {
+              float xf[8];
+              unpack8<DT>(*reinterpret_cast<const uint4 *>(xs + i * KB + (lane + 32 * u) * 8), xf);
+#pragma unroll
+              for (int q = 0; q < JG; ++q) {
+                float t = acc[i][jg + q];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t = fmaf(xf[e], af[q][e], t);
+                acc[i][jg + q] = t;
+              }
+            }
+          }
+        }
+      } else if (!timed_out) {
         // No guards: A is zero outside the slice and the rank, x is zero past the slice, so
         // every chunk and rank row of the pass runs unconditionally (straight-line code).
         constexpr int CH = JPW <= 2 ? 2 : 1;
@@ -643,26 +675,29 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
         *reinterpret_cast<uint4 *>(pr.y + (int64_t)row0 * pr.ldy + n0) = pack8<DT>(yf);
       }
     } else {
+      // Several rows: per rank row, the B chunk is unpacked once and meets every row's v (a
+      // broadcast read of shared memory) in paired fp32 FMAs.
       for (int c8 = tid; c8 < n8; c8 += NTHREADS) {
         const int n0 = n_begin + c8 * 8;
-        float acc[RT][8];
+        float2 acc2[RT][4];
 #pragma unroll
         for (int i = 0; i < RT; ++i)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
-        if (b_staged) {
-          for (int j = 0; j < rank; ++j) {
-            float bf[8];
-            unpack8<DT>(*reinterpret_cast<const uint4 *>(bs + j * p.nb + c8 * 8), bf);
+          for (int e = 0; e < 4; ++e) acc2[i][e] = make_float2(0.f, 0.f);
+        auto add_row = [&](const uint4 &bw, int j) {
+          float2 b2[4];
+          unpack8x2<DT>(bw, b2);
 #pragma unroll
-            for (int i = 0; i < RT; ++i) {
-              if (i < nr) {
-                const float vij = vsm[i * p.r_alloc + j];
+          for (int i = 0; i < RT; ++i) {
+            const float vij = vsm[i * p.r_alloc + j];  // rows past nr hold garbage; never stored
+            const float2 v2 = make_float2(vij, vij);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(vij, bf[e], acc[i][e]);
-              }
-            }
+            for (int e = 0; e < 4; ++e) acc2[i][e] = __ffma2_rn(v2, b2[e], acc2[i][e]);
           }
+        };
+        if (b_staged) {
+#pragma unroll 2
+          for (int j = 0; j < rank; ++j) add_row(*reinterpret_cast<const uint4 *>(bs + j * p.nb + c8 * 8), j);
         } else {
           constexpr int UB = 4;  // B loads in flight per thread
           for (int j0 = 0; j0 < rank; j0 += UB) {
@@ -671,29 +706,21 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
             for (int u = 0; u < UB; ++u)
               if (j0 + u < rank) b[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
 #pragma unroll
-            for (int u = 0; u < UB; ++u) {
-              if (j0 + u < rank) {
-                float bf[8];
-                unpack8<DT>(b[u], bf);
-#pragma unroll
-                for (int i = 0; i < RT; ++i) {
-                  if (i < nr) {
-                    const float vij = vsm[i * p.r_alloc + j0 + u];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(vij, bf[e], acc[i][e]);
-                  }
-                }
-              }
-            }
+            for (int u = 0; u < UB; ++u)
+              if (j0 + u < rank) add_row(b[u], j0 + u);
           }
         }
 #pragma unroll
         for (int i = 0; i < RT; ++i) {
           if (i < nr) {
             float yf[8];
-            unpack8<DT>(ldg_u4(pr.y + (int64_t)(row0 + i) * pr.ldy + n0), yf);
+            unpack8<DT>(y_bulk ? *reinterpret_cast<const uint4 *>(ys + i * p.ny + c8 * 8)
+                               : ldg_u4(pr.y + (int64_t)(row0 + i) * pr.ldy + n0), yf);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) yf[e] = fmaf(scale, acc[i][e], yf[e]);
+            for (int e = 0; e < 4; ++e) {
+              yf[2 * e] = fmaf(scale, acc2[i][e].x, yf[2 * e]);
+              yf[2 * e + 1] = fmaf(scale, acc2[i][e].y, yf[2 * e + 1]);
+            }
             *reinterpret_cast<uint4 *>(pr.y + (int64_t)(row0 + i) * pr.ldy + n0) = pack8<DT>(yf);
           }
         }
@@ -758,9 +785,14 @@ cudaError_t dispatch(const DecodeParams &p, unsigned grid, size_t smem, int clus
     if (r <= 64) return launch_one<DT, MODE, 1, 8>(p, grid, smem, cluster, pdl, stream);
     return launch_one<DT, MODE, 1, 16>(p, grid, smem, cluster, pdl, stream);
   }
-  if (r <= 16) return launch_one<DT, MODE, 8, 2>(p, grid, smem, cluster, pdl, stream);
-  if (r <= 32) return launch_one<DT, MODE, 8, 4>(p, grid, smem, cluster, pdl, stream);
-  if (r <= 64) return launch_one<DT, MODE, 8, 8>(p, grid, smem, cluster, pdl, stream);
+  if (p.rt == 8) {
+    if (r <= 16) return launch_one<DT, MODE, 8, 2>(p, grid, smem, cluster, pdl, stream);
+    if (r <= 32) return launch_one<DT, MODE, 8, 4>(p, grid, smem, cluster, pdl, stream);
+    if (r <= 64) return launch_one<DT, MODE, 8, 8>(p, grid, smem, cluster, pdl, stream);
+  }
+  if (r <= 16) return launch_one<DT, MODE, 4, 2>(p, grid, smem, cluster, pdl, stream);
+  if (r <= 32) return launch_one<DT, MODE, 4, 4>(p, grid, smem, cluster, pdl, stream);
+  if (r <= 64) return launch_one<DT, MODE, 4, 8>(p, grid, smem, cluster, pdl, stream);
   return launch_one<DT, MODE, 4, 16>(p, grid, smem, cluster, pdl, stream);
 }
 

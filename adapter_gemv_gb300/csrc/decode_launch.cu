@@ -33,10 +33,12 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   }
   p.r_alloc = r_alloc;
   // Rows per tile: one row when the segments are a row or two long (decode with distinct
-  // adapters, BGMV), else 8 (4 above rank 64) so an adapter row is reused across rows.
+  // adapters, BGMV); else 4, so an adapter row is reused across rows without many empty rows in
+  // short segments; 8 when segments average 16 rows or more (ranks up to 64).
   const bool sgmv = p.seg_off != nullptr;
-  const bool multi = sgmv && p.M >= 2 * (p.nseg > 0 ? p.nseg : 1);
-  p.rt = multi ? (r_alloc <= 64 ? 8 : 4) : 1;
+  const int nseg1 = p.nseg > 0 ? p.nseg : 1;
+  const bool multi = sgmv && p.M >= 2 * nseg1;
+  p.rt = !multi ? 1 : (p.M >= 16 * nseg1 && r_alloc <= 64) ? 8 : 4;
   int64_t tiles = !sgmv ? (int64_t)p.M : (p.rt == 1 ? (int64_t)p.M : (int64_t)p.nseg + (p.M + p.rt - 1) / p.rt);
   if (sgmv && p.tc_min > 0) {
     // only segments shorter than tc_min rows are left for these kernels
@@ -80,11 +82,11 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   p.nb = (mode != MODE_SHRINK && (int64_t)r_alloc * nchunk * 2 <= b_cap) ? nchunk : 0;
   p.kb = kb;
   p.spare = 0;
-  // One-row tiles also take their y slice into shared memory, if the CTA stays small enough
-  // to share an SM with another.
+  // The tile's y rows also go to shared memory, if the CTA stays small enough to share an SM
+  // with another.
   const int lcs = (mode == MODE_EXPAND) ? 1 : cs;
   p.ny = 0;
-  if (p.rt == 1 && mode != MODE_SHRINK && nchunk * 2 <= y_cap &&
+  if (mode != MODE_SHRINK && p.rt * nchunk * 2 <= y_cap &&
       Layout::make(lcs, p.rt, r_alloc, kb, p.nb, nchunk).total <= y_total_cap)
     p.ny = nchunk;
   const Layout L = Layout::make(lcs, p.rt, r_alloc, kb, p.nb, p.ny);
