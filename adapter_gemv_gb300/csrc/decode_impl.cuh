@@ -785,11 +785,6 @@ cudaError_t dispatch(const DecodeParams &p, unsigned grid, size_t smem, int clus
     if (r <= 64) return launch_one<DT, MODE, 1, 8>(p, grid, smem, cluster, pdl, stream);
     return launch_one<DT, MODE, 1, 16>(p, grid, smem, cluster, pdl, stream);
   }
-  if (p.rt == 8) {
-    if (r <= 16) return launch_one<DT, MODE, 8, 2>(p, grid, smem, cluster, pdl, stream);
-    if (r <= 32) return launch_one<DT, MODE, 8, 4>(p, grid, smem, cluster, pdl, stream);
-    if (r <= 64) return launch_one<DT, MODE, 8, 8>(p, grid, smem, cluster, pdl, stream);
-  }
   if (r <= 16) return launch_one<DT, MODE, 4, 2>(p, grid, smem, cluster, pdl, stream);
   if (r <= 32) return launch_one<DT, MODE, 4, 4>(p, grid, smem, cluster, pdl, stream);
   if (r <= 64) return launch_one<DT, MODE, 4, 8>(p, grid, smem, cluster, pdl, stream);

@@ -33,12 +33,11 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   }
   p.r_alloc = r_alloc;
   // Rows per tile: one row when the segments are a row or two long (decode with distinct
-  // adapters, BGMV); else 4, so an adapter row is reused across rows without many empty rows in
-  // short segments; 8 when segments average 16 rows or more (ranks up to 64).
+  // adapters, BGMV), else 4 (an adapter row is reused across 4 rows; measured faster than 8 on
+  // decode steps, whose longer tiles cost more registers and more empty rows).
   const bool sgmv = p.seg_off != nullptr;
-  const int nseg1 = p.nseg > 0 ? p.nseg : 1;
-  const bool multi = sgmv && p.M >= 2 * nseg1;
-  p.rt = !multi ? 1 : (p.M >= 16 * nseg1 && r_alloc <= 64) ? 8 : 4;
+  const bool multi = sgmv && p.M >= 2 * (p.nseg > 0 ? p.nseg : 1);
+  p.rt = multi ? 4 : 1;
   int64_t tiles = !sgmv ? (int64_t)p.M : (p.rt == 1 ? (int64_t)p.M : (int64_t)p.nseg + (p.M + p.rt - 1) / p.rt);
   if (sgmv && p.tc_min > 0) {
     // only segments shorter than tc_min rows are left for these kernels
@@ -65,6 +64,10 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   if (mode != MODE_EXPAND) cs_min = (d_in_max + kb - 1) / kb;
   if (mode != MODE_SHRINK) {
     const int need = (int)(((int64_t)r_alloc * d_out_max * 2 + b_cap - 1) / b_cap);
+    cs_min = cs_min > need ? cs_min : need;
+  }
+  if (p.rt > 1 && mode != MODE_SHRINK) {  // one pass of the expand loop per thread
+    const int need = (d_out_max + 8 * decode::NTHREADS - 1) / (8 * decode::NTHREADS);
     cs_min = cs_min > need ? cs_min : need;
   }
   int cs = (int)((sms / 2 + units - 1) / units);
