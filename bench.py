@@ -140,8 +140,9 @@ class ClockSampler:
 
 
 def kernel_source_hash():
+    """Hash of the decode kernel's sources: a committed ncu traffic figure counts only for them."""
     h = hashlib.sha256()
-    for f in ("decode.cu", "common.cuh", "launch.h"):
+    for f in ("decode_impl.cuh", "decode_fused.cu", "decode_launch.cu", "common.cuh", "launch.h"):
         h.update(open(os.path.join(ROOT, "adapter_gemv_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
