@@ -59,7 +59,7 @@ struct TcParams {
   int32_t *status;
   int32_t tc_min;  // segments of at least this many rows are this path's
   // chosen by the launcher
-  int32_t rpad, ksplit, tiles, nper, nblk_total, tmem_cols;
+  int32_t rpad, ksplit, tiles, nper, nblk_total, tmem_cols, stages;
 };
 
 constexpr int kTcMinRows = 32;

@@ -30,7 +30,7 @@ namespace {
 
 constexpr int BM = 128;      // rows per tile (MMA M)
 constexpr int BK = 64;       // K elements per stage (one 128-byte swizzle row)
-constexpr int STAGES = 4;    // shrink ring depth
+constexpr int MAX_STAGES = 12;  // shrink ring depth: as many stages as fit, up to this
 constexpr int EBUF = 3;      // expand pipeline buffers
 constexpr int NTHREADS = 128;
 constexpr int SCAN_CAP = 512;
@@ -124,13 +124,17 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 // shrink
 
 struct ShrinkSmem {
-  int stage_bytes, a_off, bar_off, total;
-  __host__ __device__ static ShrinkSmem make(int rpad) {
+  int stages, stage_bytes, a_off, bar_off, total;
+  // stages = 0: as many as fit in 227 KB (a deep ring keeps one CTA's TMA loads streaming)
+  __host__ __device__ static ShrinkSmem make(int rpad, int stages = 0) {
     ShrinkSmem L;
     L.a_off = BM * BK * 2;                                   // X tile: 16 KB
     L.stage_bytes = (L.a_off + rpad * BK * 2 + 1023) & ~1023;  // + A^T rows
-    L.bar_off = STAGES * L.stage_bytes;
-    L.total = L.bar_off + 1024 + (2 * SCAN_CAP + 1) * 4 + 1024;  // barriers, tile info, scan, alignment slack
+    const int fixed = 1024 + (2 * SCAN_CAP + 1) * 4 + 1024;   // barriers, tile info, scan, alignment slack
+    if (stages <= 0) stages = (227 * 1024 - fixed) / L.stage_bytes;
+    L.stages = stages < 2 ? 2 : stages > MAX_STAGES ? MAX_STAGES : stages;
+    L.bar_off = L.stages * L.stage_bytes;
+    L.total = L.bar_off + fixed;
     return L;
   }
 };
@@ -141,10 +145,11 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
                                                              const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  const ShrinkSmem L = ShrinkSmem::make(p.rpad);
+  const ShrinkSmem L = ShrinkSmem::make(p.rpad, p.stages);
+  const int STAGES = L.stages;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
-  uint64_t *empty = full + STAGES;
-  uint64_t *accbar = empty + STAGES;
+  uint64_t *empty = full + MAX_STAGES;
+  uint64_t *accbar = empty + MAX_STAGES;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accbar + 1);
   int32_t *flags = reinterpret_cast<int32_t *>(tmem_slot + 1);  // [0] = timed out
   TcTile *ti = reinterpret_cast<TcTile *>(smem + L.bar_off + 256);
@@ -595,8 +600,15 @@ cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stre
   p.tiles = p.M / BM + p.nseg;  // >= sum over long segments of ceil(len / 128)
   if (p.tiles <= 0) return cudaSuccess;
   const int kb_total = (pl.d_in + BK - 1) / BK;
-  // K split: as many parts as keep the whole grid resident at two CTAs per SM (one wave)
-  int ks = 2 * sm_count_tc() / (p.tiles > 0 ? p.tiles : 1);
+  p.stages = ShrinkSmem::make(p.rpad).stages;
+  const size_t smem = ShrinkSmem::make(p.rpad, p.stages).total;
+  auto kern = tc_shrink_kernel<MLORA_BF16>;
+  cudaError_t e = set_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  // K split: as many parts as keep the whole grid resident (one wave)
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NTHREADS, smem) != cudaSuccess || occ < 1) occ = 1;
+  int ks = occ * sm_count_tc() / (p.tiles > 0 ? p.tiles : 1);
   ks = ks < 1 ? 1 : ks > 4 ? 4 : ks;
   ks = ks > kb_total ? kb_total : ks;
   p.ksplit = ks;
@@ -604,10 +616,6 @@ cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stre
   if (!encode_2d(&tm_x, pl.dtype, pr.x, pl.d_in, p.M, pr.ldx, BM)) return cudaErrorInvalidValue;
   if (!encode_2d(&tm_a, pl.dtype, pl.a_t, pl.d_in, (int64_t)pl.num_slots * pl.num_layers * pl.r_max, pl.d_in, p.rpad))
     return cudaErrorInvalidValue;
-  const size_t smem = ShrinkSmem::make(p.rpad).total;
-  auto kern = tc_shrink_kernel<MLORA_BF16>;
-  cudaError_t e = set_smem(kern, smem);
-  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ks, p.tiles, 1);
   cfg.blockDim = dim3(NTHREADS, 1, 1);
