@@ -31,7 +31,7 @@ namespace {
 constexpr int BM = 128;      // rows per tile (MMA M)
 constexpr int BK = 64;       // K elements per stage (one 128-byte swizzle row)
 constexpr int MAX_STAGES = 12;  // shrink ring depth: as many stages as fit, up to this
-constexpr int EBUF = 3;      // expand pipeline buffers
+constexpr int MAX_EBUF = 8;  // expand pipeline buffers: as many as fit with two CTAs per SM, up to this
 constexpr int NTHREADS = 128;
 constexpr int SCAN_CAP = 512;
 
@@ -281,26 +281,31 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
 // ------------------------------------------------------------------------------------------
 // expand
 
-// Warp roles: warps 0-3 (128 threads, TMEM lanes 0-127) build V and run the epilogue, one y row
-// each; warp 4 lane 0 loads (TMA) the y tile and B rows of each 64-column block into a ring of
-// EBUF buffers; warp 5 lane 0 issues the MMAs into one of two TMEM accumulators, so a block's
-// MMA overlaps the previous block's epilogue.
-constexpr int EXP_EPI_WARPS = 4;
+// Warp roles: warps 0-7 run the epilogue -- warp w reads TMEM lanes 32 (w % 4) .. +31 (its 32 y
+// rows) and the block's columns 32 (w / 4) .. +31; warps 0-3 also build V, one row per thread;
+// warp 8 lane 0 loads (TMA) the y tile and B rows of each 64-column block into a ring of
+// buffers; warp 9 lane 0 issues the MMAs into one of two TMEM accumulators, so a block's MMA
+// overlaps the previous block's epilogue.
+constexpr int EXP_EPI_WARPS = 8;
 constexpr int EXP_THREADS = (EXP_EPI_WARPS + 2) * 32;
 
 // Shared memory: V hi / lo, then EBUF pipeline buffers, each with the y tile of one 64-column
 // block (128 rows x 128 B) followed by its B rows (one MN atom: rpad K rows x 128 B).
 struct ExpandSmem {
-  int v_off, buf_off, buf_bytes, b_in_buf, bar_off, total;
-  __host__ __device__ static ExpandSmem make(int rpad) {
+  int nbuf, v_off, buf_off, buf_bytes, b_in_buf, bar_off, total;
+  // nbuf = 0: as many buffers as fit in `budget` bytes
+  __host__ __device__ static ExpandSmem make(int rpad, int nbuf = 0, int budget = 227 * 1024) {
     ExpandSmem L;
     const int katoms = (rpad + BK - 1) / BK;
     L.v_off = 0;
     L.buf_off = 2 * katoms * BM * 128;
     L.b_in_buf = BM * 128;
     L.buf_bytes = (L.b_in_buf + rpad * 128 + 1023) & ~1023;
-    L.bar_off = L.buf_off + EBUF * L.buf_bytes;
-    L.total = L.bar_off + 1024 + (2 * SCAN_CAP + 1) * 4 + 1024;
+    const int fixed = 1024 + (2 * SCAN_CAP + 1) * 4 + 1024;
+    if (nbuf <= 0) nbuf = (budget - fixed - L.buf_off) / L.buf_bytes;
+    L.nbuf = nbuf < 2 ? 2 : nbuf > MAX_EBUF ? MAX_EBUF : nbuf;
+    L.bar_off = L.buf_off + L.nbuf * L.buf_bytes;
+    L.total = L.bar_off + fixed;
     return L;
   }
 };
@@ -329,11 +334,12 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
                                                                 const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  const ExpandSmem L = ExpandSmem::make(p.rpad);
+  const ExpandSmem L = ExpandSmem::make(p.rpad, p.stages);
+  const int EBUF = L.nbuf;
   const int katoms = (p.rpad + BK - 1) / BK;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);  // [EBUF] y tile + B rows landed
-  uint64_t *empty = full + EBUF;      // [EBUF] the buffer's y tile has been stored (or written)
-  uint64_t *accfull = empty + EBUF;   // [2] accumulator a holds a finished block
+  uint64_t *empty = full + MAX_EBUF;      // [EBUF] the buffer's y tile has been stored (or written)
+  uint64_t *accfull = empty + MAX_EBUF;   // [2] accumulator a holds a finished block
   uint64_t *accempty = accfull + 2;   // [2] the epilogue has read accumulator a
   uint64_t *mmadone = accempty + 2;   // every MMA this CTA issued has completed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mmadone + 1);
@@ -393,7 +399,7 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
     for (; issued < nblk && issued < EBUF; ++issued) issue(issued);
 
   // V hi / lo in the K-major 128-byte-swizzle layout: epilogue thread m owns row m
-  if (active && warp < EXP_EPI_WARPS) {
+  if (active && warp < 4) {
     const int m = tid;
     const float *vrow = p.v + (int64_t)(row0 + (m < nr ? m : 0)) * p.r_max;
     const bool vec = ((p.r_max & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.v) & 15) == 0);
@@ -478,8 +484,8 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
     }
     __syncwarp();
   } else if (active) {
-    // ---- epilogue: row m of the block's y tile += scale * D, rounded once
-    const int m = tid;
+    // ---- epilogue: row m of the block's y tile += scale * D (this warp's 32 columns), rounded once
+    const int m = (warp & 3) * 32 + lane, half = warp >> 2;
     int i = 0;
     for (; i < nblk; ++i) {
       const int a = i & 1, nb = nb_begin + i;
@@ -489,23 +495,24 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
       if (!ok) flags[0] = 1;
       if (epi_sync_or(!ok || flags[0])) break;  // the same decision in every epilogue thread
       tc::tc_fence_after();
-      float d[EBN];
+      float d[EBN / 2];
 #pragma unroll
-      for (int c16 = 0; c16 < EBN / 16; ++c16) {
+      for (int c16 = 0; c16 < EBN / 32; ++c16) {
         float q[16];
-        tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(a * EBN + c16 * 16), q);
+        tc::tmem_ld16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(a * EBN + half * (EBN / 2) + c16 * 16), q);
 #pragma unroll
         for (int e = 0; e < 16; ++e) d[c16 * 16 + e] = q[e];
       }
       tc::tc_fence_before();
       mbar_arrive(&accempty[a]);  // the accumulator may take the block after next
 #pragma unroll
-      for (int ch = 0; ch < EBN / 8; ++ch) {  // 16-byte chunks of the 128-byte row
+      for (int cq = 0; cq < EBN / 16; ++cq) {  // this warp's 16-byte chunks of the 128-byte row
+        const int ch = half * (EBN / 16) + cq;
         uint4 *cell = reinterpret_cast<uint4 *>(ys + m * 128 + ((ch ^ (m & 7)) << 4));
         float yf[8];
         unpack8<DT>(*cell, yf);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) yf[e] = fmaf(scale, d[ch * 8 + e], yf[e]);
+        for (int e = 0; e < 8; ++e) yf[e] = fmaf(scale, d[cq * 8 + e], yf[e]);
         if (full_tile) {
           *cell = pack8<DT>(yf);
         } else if (m < nr && nb * EBN + ch * 8 < p.d_out) {
@@ -638,14 +645,16 @@ cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stre
   p.tiles = p.M / BM + p.nseg;
   if (p.tiles <= 0) return cudaSuccess;
   p.nblk_total = (pl.d_out + EBN - 1) / EBN;
-  // 16 blocks of 64 columns per CTA: measured best on the 13B prefill (1024 columns per CTA,
-  // three blocks in flight; shorter runs pay the V setup more often, longer ones leave SMs idle)
+  // 16 blocks of 64 columns per CTA: measured best on the 13B prefill (1024 columns per CTA;
+  // shorter runs pay the V setup more often, longer ones leave SMs idle)
   p.nper = 16;
+  const int expand_budget = 112 * 1024;  // two CTAs per SM
   CUtensorMap tm_b, tm_y;
   if (!encode_2d(&tm_b, pl.dtype, pl.b, pl.d_out, (int64_t)pl.num_slots * pl.num_layers * pl.r_max, pl.d_out, p.rpad))
     return cudaErrorInvalidValue;
   if (!encode_2d(&tm_y, pl.dtype, pr.y, pl.d_out, p.M, pr.ldy, BM)) return cudaErrorInvalidValue;
-  const size_t smem = ExpandSmem::make(p.rpad).total;
+  p.stages = ExpandSmem::make(p.rpad, 0, expand_budget).nbuf;
+  const size_t smem = ExpandSmem::make(p.rpad, p.stages).total;
   auto kern = tc_expand_kernel<MLORA_BF16>;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
