@@ -70,6 +70,11 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
     const int need = (d_out_max + 8 * decode::NTHREADS - 1) / (8 * decode::NTHREADS);
     cs_min = cs_min > need ? cs_min : need;
   }
+  // ... but no split that makes the grid more than about four waves of resident CTAs (two per
+  // SM): past that, CTAs that loop over several passes of A beat more, shorter CTAs
+  // (Llama-2-70B q_proj, rank 64, 256 rows: 16 CTAs per row 211 us, 4 CTAs per row 120 us).
+  const int64_t cs_cap = (8 * (int64_t)sms) / units;
+  if (cs_min > cs_cap) cs_min = cs_cap > 1 ? (int)cs_cap : 1;
   int cs = (int)((sms / 2 + units - 1) / units);
   cs = cs > cs_min ? cs : cs_min;
   const int split_dim = (mode == MODE_EXPAND) ? d_out_max : d_in_max;
