@@ -223,7 +223,7 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
 //   [64, 96)     TileInfo
 //   gbuf         [cs][RT][r_alloc] floats: every CTA's partial v (cluster modes)
 //   vsm          [RT][r_alloc] floats: the summed v of the tile
-//   xs           [RT][kb] elements: one pass of the tile's x rows (shrink)
+//   xs           [RT][max(kb, xw)] elements: the tile's x rows, one pass or the whole slice (shrink)
 //   ys           [RT][ny] elements: the y rows' slices, when staged (expand)
 //   then one region used twice:
 //     while resolving the tile: scan [2 * SCAN_CAP + 1] ints (segment offsets and slots) and
@@ -233,12 +233,12 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
 //   the neighbouring launch.
 struct Layout {
   int gbuf, vsm, xs, ys, scan, rank_c, scale_c, bs, total;
-  __host__ __device__ static Layout make(int cs, int rt, int r_alloc, int kb, int nb_staged, int ny) {
+  __host__ __device__ static Layout make(int cs, int rt, int r_alloc, int kb, int nb_staged, int ny, int xw) {
     Layout L;
     L.gbuf = 128;
     L.vsm = L.gbuf + cs * rt * r_alloc * 4;
     L.xs = (L.vsm + rt * r_alloc * 4 + 127) & ~127;
-    L.ys = (L.xs + rt * kb * 2 + 127) & ~127;
+    L.ys = (L.xs + rt * (xw > kb ? xw : kb) * 2 + 127) & ~127;
     L.scan = (L.ys + rt * ny * 2 + 127) & ~127;
     L.rank_c = L.scan + (2 * SCAN_CAP + 1) * 4;
     L.scale_c = L.rank_c + RANK_CACHE * 4;
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   constexpr int KB = Pass<JPW>::KB;
   const int cs = p.csplit;  // CTAs per tile: the cluster (SHRINK, FUSED) or the N-split (EXPAND)
   const bool stage_b = p.nb > 0;  // B rows of the CTA's slice go to shared memory before the wait
-  const Layout L = Layout::make(MODE == MODE_EXPAND ? 1 : cs, RT, p.r_alloc, KB, p.nb, p.ny);
+  const Layout L = Layout::make(MODE == MODE_EXPAND ? 1 : cs, RT, p.r_alloc, KB, p.nb, p.ny, p.xw);
   uint64_t *xbar = reinterpret_cast<uint64_t *>(smem);
   uint64_t *bbar = xbar + 1;
   uint64_t *ibar = xbar + 2;
@@ -315,9 +315,12 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   const bool do_shrink = MODE != MODE_EXPAND && active;
   const bool do_expand = MODE != MODE_SHRINK && active;
   const bool b_staged = do_expand && stage_b && n_end > n_begin;
-  // Tiles whose d_in slice is a single pass take their x rows (and, when the launcher made
-  // room, their y rows) into shared memory by bulk copies issued right after the wait.
-  const bool x_bulk = do_shrink && k_end > k_begin && k_end - k_begin <= KB;
+  // Tiles whose d_in slice fits xs take their x rows (and, when the launcher made room, their
+  // y rows) into shared memory by bulk copies issued right after the wait.
+  // xs holds XW elements of each row: the CTA's whole d_in slice when the launcher made room
+  // (p.xw > 0), else one pass (KB); the whole-slice form is filled by bulk copies.
+  const int XW = p.xw > 0 ? p.xw : KB;
+  const bool x_bulk = do_shrink && k_end > k_begin && k_end - k_begin <= XW;
   const bool y_bulk = do_expand && p.ny > 0 && n_end > n_begin;
   const uint64_t evict_first = policy_evict_first();
 
@@ -393,9 +396,9 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   if (do_shrink) load_a(k_begin);
   if (x_bulk) {  // the bulk copies fill xs rows < nr up to the slice end; zeros elsewhere (disjoint bytes)
     const int s8 = (k_end - k_begin) >> 3;
-    for (int e = tid; e < RT * (KB / 8); e += NTHREADS) {
-      const int i = e / (KB / 8), c8 = e % (KB / 8);
-      if (i >= nr || c8 >= s8) *reinterpret_cast<uint4 *>(xs + i * KB + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
+    for (int e = tid; e < RT * (XW / 8); e += NTHREADS) {
+      const int i = e / (XW / 8), c8 = e % (XW / 8);
+      if (i >= nr || c8 >= s8) *reinterpret_cast<uint4 *>(xs + i * XW + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
 
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
     if (x_bulk) {
       mbar_arrive_expect_tx(ibar, (uint32_t)(nr * (k_end - k_begin) * 2));
       for (int i = 0; i < nr; ++i)
-        bulk_g2s(xs + i * KB, pr.x + (int64_t)(row0 + i) * pr.ldx + k_begin, (uint32_t)(k_end - k_begin) * 2, ibar);
+        bulk_g2s(xs + i * XW, pr.x + (int64_t)(row0 + i) * pr.ldx + k_begin, (uint32_t)(k_end - k_begin) * 2, ibar);
     }
     if (y_bulk) {
       mbar_arrive_expect_tx(ybar, (uint32_t)(nr * (n_end - n_begin) * 2));
@@ -423,7 +426,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
 #pragma unroll
       for (int jj = 0; jj < JPW; ++jj) acc[i][jj] = 0.f;
 
-    if (x_bulk) {
+    if (x_bulk && k_end - k_begin <= KB) {
       // One row, one pass: each lane reads its x chunks from shared memory, unpacks each once
       // for all its rank rows and accumulates pairs of products with the paired fp32 FMA (two
       // independent chains per rank row when a warp has at most 2 rank rows).
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
 #pragma unroll
             for (int i = 0; i < RT; ++i) {
               float xf[8];
-              unpack8<DT>(*reinterpret_cast<const uint4 *>(xs + i * KB + (lane + 32 * u) * 8), xf);
+              unpack8<DT>(*reinterpret_cast<const uint4 *>(xs + i * XW + (lane + 32 * u) * 8), xf);
 #pragma unroll
               for (int q = 0; q < JG; ++q) {
                 float t = acc[i][jg + q];
@@ -476,6 +479,45 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
             for (int e = 0; e < 4; ++e) acc2[jj][e % CH] = __ffma2_rn(x2[e], a2[e], acc2[jj][e % CH]);
           }
         }
+#pragma unroll
+        for (int jj = 0; jj < JPW; ++jj) {
+          float2 t2 = acc2[jj][0];
+#pragma unroll
+          for (int h = 1; h < CH; ++h) t2 = make_float2(t2.x + acc2[jj][h].x, t2.y + acc2[jj][h].y);
+          acc[0][jj] = t2.x + t2.y;
+        }
+      }
+    } else if (x_bulk && RT == 1) {
+      // The x slice is in shared memory; A comes in passes of KB elements (the first loaded into
+      // registers before the wait, the next ones from L2, where they were prefetched). No
+      // guards: A is zero outside the slice and the rank, x is zero past the slice and nr.
+      const int ok = mbar_wait(ibar, 0) ? 1 : 0;
+      timed_out = __syncthreads_or(!ok);
+      constexpr int CH = JPW <= 2 ? 2 : 1;
+      float2 acc2[JPW][CH];  // one-row tiles: pairs of products, CH independent chains per rank row
+#pragma unroll
+      for (int jj = 0; jj < JPW; ++jj)
+#pragma unroll
+        for (int h = 0; h < CH; ++h) acc2[jj][h] = make_float2(0.f, 0.f);
+      for (int pass = 0; !timed_out && pass * KB < k_end - k_begin; ++pass) {
+        if (pass > 0) load_a(k_begin + pass * KB);
+        const uint16_t *xp = xs + pass * KB;
+          // One row: each lane unpacks its x chunk once for all its rank rows and accumulates
+          // pairs of products with the paired fp32 FMA.
+#pragma unroll
+          for (int u = 0; u < UK; ++u) {
+            float2 x2[4];
+            unpack8x2<DT>(*reinterpret_cast<const uint4 *>(xp + (lane + 32 * u) * 8), x2);
+#pragma unroll
+            for (int jj = 0; jj < JPW; ++jj) {
+              float2 a2[4];
+              unpack8x2<DT>(a[jj][u], a2);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc2[jj][e % CH] = __ffma2_rn(x2[e], a2[e], acc2[jj][e % CH]);
+            }
+          }
+      }
+      {
 #pragma unroll
         for (int jj = 0; jj < JPW; ++jj) {
           float2 t2 = acc2[jj][0];

@@ -89,15 +89,21 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   const int nchunk = ((d_out_max + cs - 1) / cs + 7) & ~7;
   p.nb = (mode != MODE_SHRINK && (int64_t)r_alloc * nchunk * 2 <= b_cap) ? nchunk : 0;
   p.kb = kb;
-  p.spare = 0;
+  // The x row of a one-row tile whose d_in slice spans several passes of A goes to shared
+  // memory whole, when it fits in 32 KB; each pass then reads its part there.
+  {
+    const int kchunk = ((d_in_max + cs - 1) / cs + 7) & ~7;
+    const int npass = (kchunk + kb - 1) / kb;
+    p.xw = (mode != MODE_EXPAND && p.rt == 1 && npass > 1 && npass * kb * 2 <= 32 * 1024) ? npass * kb : 0;
+  }
   // The tile's y rows also go to shared memory, if the CTA stays small enough to share an SM
   // with another.
   const int lcs = (mode == MODE_EXPAND) ? 1 : cs;
   p.ny = 0;
   if (mode != MODE_SHRINK && p.rt * nchunk * 2 <= y_cap &&
-      Layout::make(lcs, p.rt, r_alloc, kb, p.nb, nchunk).total <= y_total_cap)
+      Layout::make(lcs, p.rt, r_alloc, kb, p.nb, nchunk, p.xw).total <= y_total_cap)
     p.ny = nchunk;
-  const Layout L = Layout::make(lcs, p.rt, r_alloc, kb, p.nb, p.ny);
+  const Layout L = Layout::make(lcs, p.rt, r_alloc, kb, p.nb, p.ny, p.xw);
   if (L.total > 227 * 1024) return cudaErrorInvalidConfiguration;
 
   const int64_t grid = units * cs;

@@ -43,7 +43,8 @@ struct DecodeParams {
   int32_t tc_min;  // > 0: segments of at least tc_min rows are done by the tensor-core kernels;
                    // these kernels take only the shorter segments
   // chosen by the launcher
-  int32_t rt, tiles, csplit, kb, nb, ny, spare, r_alloc;  // nb: staged B columns; ny: y slice staged
+  int32_t rt, tiles, csplit, kb, nb, ny, xw, r_alloc;  // nb: staged B columns; ny: y slice staged;
+                                                      // xw: x row width staged (whole d_in slice), 0 = one pass
 };
 
 // Tensor-core path for the full 128-row blocks of long SGMV segments (prefill_tc.cu).
