@@ -609,6 +609,10 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
           }
         }
       }
+      // Second cluster phase: every push into this CTA has landed (or the wait gave up), so it
+      // needs nothing more from its peers. A CTA leaves only after all peers have arrived, i.e.
+      // after every push in the cluster has landed; the early arrival spares the wait at exit.
+      cluster_arrive_release();
     } else if (do_shrink && !timed_out && lane == 0) {
 #pragma unroll
       for (int jj = 0; jj < JPW; ++jj) {
@@ -777,7 +781,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
     if (y_bulk) (void)mbar_wait(ybar, 0, 100000000ull);
     if (tid == 0) report(p.status, MLORA_STATUS_TIMEOUT);
   }
-  if (clustered) cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
+  if (clustered) cluster_wait();  // no CTA leaves while a peer may still write into its shared memory
 }
 
 // Host: launch one instantiation with the cluster and PDL attributes.
