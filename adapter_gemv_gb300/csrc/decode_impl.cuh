@@ -669,7 +669,13 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
         };
         constexpr int UB = 8;  // B rows in flight per thread when they come from global memory
         if constexpr (VREG) {
-          if (b_staged) {
+          if (b_staged && rank == RV) {  // every rank row present: straight-line, no guards
+#pragma unroll
+            for (int j = 0; j < RV; j += 2) {
+              add_row(*reinterpret_cast<const uint4 *>(bs + j * p.nb + c8 * 8), vr[j], ev);
+              add_row(*reinterpret_cast<const uint4 *>(bs + (j + 1) * p.nb + c8 * 8), vr[j + 1], od);
+            }
+          } else if (b_staged) {
 #pragma unroll
             for (int j = 0; j < RV; j += 2) {
               if (j < rank) add_row(*reinterpret_cast<const uint4 *>(bs + j * p.nb + c8 * 8), vr[j], ev);
