@@ -747,7 +747,11 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
             for (int e = 0; e < 4; ++e) acc2[i][e] = __ffma2_rn(v2, b2[e], acc2[i][e]);
           }
         };
-        if (b_staged) {
+        constexpr int RF = 8 * JPW;  // largest rank of this instantiation
+        if (b_staged && rank == RF && RF <= 16) {  // every rank row present: straight-line, no guards
+#pragma unroll
+          for (int j = 0; j < RF; ++j) add_row(*reinterpret_cast<const uint4 *>(bs + j * p.nb + c8 * 8), j);
+        } else if (b_staged) {
 #pragma unroll 2
           for (int j = 0; j < rank; ++j) add_row(*reinterpret_cast<const uint4 *>(bs + j * p.nb + c8 * 8), j);
         } else {
