@@ -685,13 +685,23 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
 #pragma unroll
             for (int j0 = 0; j0 < RV; j0 += UB) {
               uint4 bq[UB];
+              if (j0 + UB <= rank) {  // a whole batch of rank rows: no guards
 #pragma unroll
-              for (int u = 0; u < UB; ++u)
-                if (j0 + u < rank) bq[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+                for (int u = 0; u < UB; ++u) bq[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
 #pragma unroll
-              for (int u = 0; u < UB; u += 2) {
-                if (j0 + u < rank) add_row(bq[u], vr[j0 + u], ev);
-                if (j0 + u + 1 < rank) add_row(bq[u + 1], vr[j0 + u + 1], od);
+                for (int u = 0; u < UB; u += 2) {
+                  add_row(bq[u], vr[j0 + u], ev);
+                  add_row(bq[u + 1], vr[j0 + u + 1], od);
+                }
+              } else if (j0 < rank) {
+#pragma unroll
+                for (int u = 0; u < UB; ++u)
+                  if (j0 + u < rank) bq[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+#pragma unroll
+                for (int u = 0; u < UB; u += 2) {
+                  if (j0 + u < rank) add_row(bq[u], vr[j0 + u], ev);
+                  if (j0 + u + 1 < rank) add_row(bq[u + 1], vr[j0 + u + 1], od);
+                }
               }
             }
           }
@@ -705,13 +715,23 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
           } else {
             for (int j0 = 0; j0 < rank; j0 += UB) {
               uint4 bq[UB];
+              if (j0 + UB <= rank) {  // a whole batch of rank rows: no guards
 #pragma unroll
-              for (int u = 0; u < UB; ++u)
-                if (j0 + u < rank) bq[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+                for (int u = 0; u < UB; ++u) bq[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
 #pragma unroll
-              for (int u = 0; u < UB; u += 2) {
-                if (j0 + u < rank) add_row(bq[u], vsm[j0 + u], ev);
-                if (j0 + u + 1 < rank) add_row(bq[u + 1], vsm[j0 + u + 1], od);
+                for (int u = 0; u < UB; u += 2) {
+                  add_row(bq[u], vsm[j0 + u], ev);
+                  add_row(bq[u + 1], vsm[j0 + u + 1], od);
+                }
+              } else {
+#pragma unroll
+                for (int u = 0; u < UB; ++u)
+                  if (j0 + u < rank) bq[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+#pragma unroll
+                for (int u = 0; u < UB; u += 2) {
+                  if (j0 + u < rank) add_row(bq[u], vsm[j0 + u], ev);
+                  if (j0 + u + 1 < rank) add_row(bq[u + 1], vsm[j0 + u + 1], od);
+                }
               }
             }
           }
