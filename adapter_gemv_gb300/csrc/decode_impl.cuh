@@ -113,7 +113,34 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
     ti->nr = 0;
   }
   __syncthreads();
-  if (sgmv) {
+  if (sgmv && p.rt == 1 && p.tc_min == 0 && p.nseg <= SCAN_CAP) {
+    // One-row tiles, every segment here: tile t is row t, in the segment whose offset is the last
+    // one <= t (one ballot per 32 offsets); the offsets are checked the same way.
+    if (warp == 0) {
+      const int cnt = p.nseg;
+      int le = 0, bad = 0;
+      for (int q0 = 0; q0 <= cnt; q0 += 32) {
+        const int q = q0 + lane;
+        const int32_t o = q <= cnt ? scan[q] : 0;
+        if (q < cnt) {
+          const int32_t o1 = scan[q + 1];
+          bad |= (o1 < o) | (o < 0) | (o1 > p.M);
+        }
+        le += __popc(__ballot_sync(0xffffffffu, q <= cnt && o <= t));
+      }
+      bad = __any_sync(0xffffffffu, bad) || scan[0] != 0 || scan[cnt] != p.M;
+      if (lane == 0) {
+        if (bad) {
+          ti->bad = MLORA_STATUS_BAD_OFFSETS;
+        } else if (t < p.M && le >= 1 && le <= cnt) {
+          ti->row0 = t;
+          ti->nr = 1;
+          ti->slot = scan[SCAN_CAP + 1 + le - 1];
+          ti->skip = 0;
+        }
+      }
+    }
+  } else if (sgmv) {
     int32_t carry = 0, found = 0, bad = 0;
     for (int base = 0; base < p.nseg; base += SCAN_CAP) {
       const int cnt = min(SCAN_CAP, p.nseg - base);
