@@ -53,7 +53,7 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   const int kb = 256 * (16 / jpw);
   // CTAs per tile (cs): the smallest split whose CTA slice of d_in is one pass of A loads and
   // whose slice of B fits in 88 KB of shared memory (so two CTAs fit on an SM), raised until
-  // the launch has at least half as many CTAs as there are SMs; at least 256 elements of the
+  // the launch has at least a third (chained calls) or half as many CTAs as there are SMs; at least 256 elements of the
   // split dimension per CTA; at most 16 per cluster. Fewer, fuller CTAs leave SM room for the
   // next launch's CTAs (programmatic dependent launch) to start and fetch their adapter rows
   // while this one runs.
@@ -75,7 +75,10 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   // (Llama-2-70B q_proj, rank 64, 256 rows: 16 CTAs per row 211 us, 4 CTAs per row 120 us).
   const int64_t cs_cap = (8 * (int64_t)sms) / units;
   if (cs_min > cs_cap) cs_min = cs_cap > 1 ? (int)cs_cap : 1;
-  int cs = (int)((sms / 2 + units - 1) / units);
+  // Chained calls (programmatic dependent launch) want fewer CTAs, so the next launch finds SM
+  // room early; a call on its own wants more, to hide its latency.
+  const int floor_ctas = pdl ? sms / 3 : sms / 2;
+  int cs = (int)((floor_ctas + units - 1) / units);
   cs = cs > cs_min ? cs : cs_min;
   const int split_dim = (mode == MODE_EXPAND) ? d_out_max : d_in_max;
   const int max_cs = split_dim / 256 > 1 ? split_dim / 256 : 1;
