@@ -15,16 +15,21 @@
 //   * Output-split expand (Punica section 3.4, "SGMV-expand schedule"): each CTA owns a slice of
 //     d_out, streams B[s] rows for that slice once per tile and rewrites y in place.
 //   * FUSED mode does both in one launch; v never leaves the chip.
-//   * Every byte a CTA needs is requested into L2 at CTA start with bulk prefetches
-//     (cp.async.bulk.prefetch.L2): HBM traffic begins at once, costs no shared memory, and
-//     -- with programmatic dependent launch -- runs ahead of griddepcontrol.wait, overlapping
-//     the previous kernel. The arithmetic then reads L2 with coalesced 16-byte loads; only a
-//     block of x rows and the exchange buffers live in shared memory, so many CTAs fit per SM.
+//   * Staging. Before griddepcontrol.wait a CTA resolves its tile (one round trip for the row
+//     metadata and the pool's rank table), loads its first pass of A rows into registers (zero
+//     outside the slice and the rank) and bulk-copies its B rows into shared memory, over the
+//     area the resolve used: the adapter rows stream in while the previous kernel runs. After
+//     the wait one thread bulk-copies the tile's x rows (and y rows, when they fit) into shared
+//     memory. Later passes of A, and B rows that do not fit, come from L2, prefetched there.
+//   * Arithmetic runs on data already on chip, as straight-line code without per-chunk or
+//     per-row guards (the staged operands are zero where they lie outside the tile), with the
+//     paired fp32 FMA.
 //   * Programmatic dependent launch (when the caller enables it): a kernel lets the next one in
-//     the stream start at once.
-//     Before griddepcontrol.wait a CTA only reads what no kernel of this library writes (the
-//     rows' metadata, the pool, the page tables); x, y and v, which the previous kernel may
-//     have written, are read after the wait (they may be prefetched into L2 before it).
+//     the stream start at once. Before griddepcontrol.wait a CTA only reads what no kernel of
+//     this library writes (the rows' metadata, the pool, the page tables); x, y and v, which the
+//     previous kernel may have written, are read after the wait (they may be prefetched into L2
+//     before it). A CTA arrives at its cluster's second barrier as soon as its exchange is done,
+//     so it can leave without waiting for its peers' expand and free its SM for the next launch.
 #pragma once
 
 #include <cuda_runtime.h>
