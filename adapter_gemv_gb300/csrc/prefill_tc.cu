@@ -524,9 +524,10 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
       if (tid == 0) {
         if (full_tile) tc::tma_store_2d(&tm_y, nb * EBN, row0, ys);  // columns past d_out are clipped
         tc::bulk_commit_group();
-        // the previous block's store has read its tile: that buffer may be refilled
-        tc::bulk_wait_group_read<1>();
-        if (i > 0) mbar_arrive(&empty[(i - 1) % EBUF]);
+        // once this block's store has read its tile (a short wait: shared memory to L2), the
+        // buffer may be refilled
+        tc::bulk_wait_group_read<0>();
+        mbar_arrive(&empty[i % EBUF]);
       }
     }
     if (tid == 0) tc::bulk_wait_group_all();  // stores complete before the shared memory goes away
