@@ -646,9 +646,14 @@ cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stre
   p.tiles = p.M / BM + p.nseg;
   if (p.tiles <= 0) return cudaSuccess;
   p.nblk_total = (pl.d_out + EBN - 1) / EBN;
-  // 16 blocks of 64 columns per CTA: measured best on the 13B prefill (1024 columns per CTA;
-  // shorter runs pay the V setup more often, longer ones leave SMs idle)
-  p.nper = 16;
+  // Column runs per tile: the grid is about two waves of the expand's two CTAs per SM (measured
+  // best on the 13B prefill: 16 blocks of 64 columns per CTA at d_out 5120, ~40 at 13824;
+  // shorter runs pay the V setup more often, longer ones leave SMs idle).
+  {
+    int runs = 4 * sm_count_tc() / (p.tiles > 0 ? p.tiles : 1);
+    runs = runs < 1 ? 1 : runs > p.nblk_total ? p.nblk_total : runs;
+    p.nper = (p.nblk_total + runs - 1) / runs;
+  }
   const int expand_budget = 112 * 1024;  // two CTAs per SM
   CUtensorMap tm_b, tm_y;
   if (!encode_2d(&tm_b, pl.dtype, pl.b, pl.d_out, (int64_t)pl.num_slots * pl.num_layers * pl.r_max, pl.d_out, p.rpad))
