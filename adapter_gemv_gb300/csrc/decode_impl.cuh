@@ -366,16 +366,6 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
     if (do_expand && n_end > n_begin) {
       for (int i = lane; i < nr; i += 32)
         prefetch_l2(pr.y + (int64_t)(row0 + i) * pr.ldy + n_begin, (uint32_t)(n_end - n_begin) * 2);
-      if (b_staged) {
-        if (lane == 0) mbar_arrive_expect_tx(bbar, (uint32_t)(rank * (n_end - n_begin) * 2));
-        __syncwarp();
-        for (int j = lane; j < rank; j += 32)
-          bulk_g2s_hint(bs + j * p.nb, b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2, bbar,
-                        evict_first);
-      } else {
-        for (int j = lane; j < rank; j += 32)
-          prefetch_l2(b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2);
-      }
     }
     if (do_shrink && k_end - k_begin > KB)
       for (int j = lane; j < rank; j += 32)
@@ -426,6 +416,18 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
     }
   };
   if (do_shrink) load_a(k_begin);
+  if (active && warp == 0 && do_expand && n_end > n_begin) {
+      if (b_staged) {
+        if (lane == 0) mbar_arrive_expect_tx(bbar, (uint32_t)(rank * (n_end - n_begin) * 2));
+        __syncwarp();
+        for (int j = lane; j < rank; j += 32)
+          bulk_g2s_hint(bs + j * p.nb, b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2, bbar,
+                        evict_first);
+      } else {
+        for (int j = lane; j < rank; j += 32)
+          prefetch_l2(b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2);
+      }
+  }
   if (x_bulk) {  // the bulk copies fill xs rows < nr up to the slice end; zeros elsewhere (disjoint bytes)
     const int s8 = (k_end - k_begin) >> 3;
     for (int e = tid; e < RT * (XW / 8); e += NTHREADS) {

@@ -81,6 +81,70 @@ def test_decode_step_with_next_call_prefetch(dev):
         check_op(op, w.batch, "sgmv", op.y, y_before=before[id(op)], what=f"prefetch {op.name} L{op.layer}")
 
 
+def ragged_rank16_step(dev, dtype, seed):
+    """Chained one-row problems whose pools have r_max 16 (the kernel that stages A in shared
+    memory): ranks 4/8/13/16 (padding rows hold NaN), d_in slices that end inside a pass of A
+    (2056, 11008), a d_out that is not a multiple of the split (1000), two rows without adapter."""
+    g = W.generator(seed, dev)
+    rng = np.random.default_rng(seed)
+    projs = [W.Projection("q", 4096, 4096), W.Projection("k", 4096, 1024), W.Projection("o", 2056, 1000),
+             W.Projection("down", 11008, 4096)]
+    num_slots, M = 24, 20
+    ranks = rng.choice(np.array([4, 8, 13, 16], np.int32), size=num_slots)
+    ranks[:4] = [4, 8, 13, 16]
+    pools = {p.name: W.stacked_pool(num_slots=num_slots, num_layers=2, r_max=16, d_in=p.d_in, d_out=p.d_out,
+                                    dtype=dtype, gen=g, device=dev, ranks=ranks) for p in projs}
+    slots = np.r_[[-1, -1], rng.permutation(num_slots)[:M - 2]].astype(np.int32)
+    slots.sort(kind="stable")
+    batch = W.batch_from_slots(slots, sgmv=True).to(dev)
+    x_qk = W.normal((M, 4096), 1.0, dtype, g, dev)
+    x_o = W.normal((M, 2056), 1.0, dtype, g, dev)
+    x_down = W.normal((M, 11008), 1.0, dtype, g, dev)
+    ops = []
+    for layer in (0, 1):
+        for p in projs:
+            x = x_qk if p.name in ("q", "k") else x_o if p.name == "o" else x_down
+            ops.append(W.Op(p.name, pools[p.name], layer, x, W.uniform((M, p.d_out), -1, 1, dtype, g, dev)))
+    return batch, ops
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_chained_rank16_step_ragged(dev, dtype):
+    """A step plan (programmatic dependent launch) over ragged rank <= 16 problems: every op on
+    every row against the oracle; rows without adapter keep their bits."""
+    batch, ops = ragged_rank16_step(dev, dtype, seed=11)
+    st = status_of(dev)
+    before = {id(op): bits(op.y) for op in ops}
+    plan = StepPlan(ops, batch, st)
+    plan()
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for op in ops:
+        check_op(op, batch, "sgmv", op.y, y_before=before[id(op)], what=f"ragged {op.name} L{op.layer}")
+
+
+def test_chained_rank16_bgmv(dev):
+    """BGMV calls issued back to back with programmatic dependent launch on (rows unsorted, two
+    without adapter), ranks below r_max: the same results as the oracle."""
+    batch, ops = ragged_rank16_step(dev, torch.bfloat16, seed=12)
+    rs = batch.row_slot.cpu().numpy()[np.random.default_rng(3).permutation(batch.M)]
+    bb = W.batch_from_slots(rs, sgmv=False).to(dev)
+    st = status_of(dev)
+    before = {id(op): bits(op.y) for op in ops}
+    handles = {id(op.pool): m.make_pool(op.pool) for op in ops}
+    v = torch.empty((bb.M, 16), dtype=torch.float32, device=dev)
+    prev = m.lora_set_programmatic_launch(True)
+    try:
+        for op in ops:
+            m.lora_bgmv(op.y, op.x, handles[id(op.pool)], bb.row_slot, op.layer, v, st)
+    finally:
+        m.lora_set_programmatic_launch(prev)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for op in ops:
+        check_op(op, bb, "bgmv", op.y, y_before=before[id(op)], what=f"bgmv chained {op.name} L{op.layer}")
+
+
 @pytest.mark.parametrize("mode", ["two_phase", "fused"])
 def test_decode_7b_single_ops(dev, mode):
     w = W.sgmv_decode_7b(device=dev, dist="skewed", num_layers=2, layers=[1])
