@@ -54,6 +54,41 @@ __device__ __forceinline__ void unpack8x2(const uint4 &u, float2 (&f)[4]) {
   f[3] = make_float2(Elem<DT>::lo(u.w), Elem<DT>::hi(u.w));
 }
 
+// Mixed-precision FMA on packed 16-bit pairs: the products of the low halves and of the high
+// halves of x and a are added in fp32 (the product of two bf16 or two fp16 values is exact in
+// fp32, so this equals unpacking both and using the fp32 FMA), one instruction per product and
+// no unpacking. mfma2: into two accumulators; mfma1: both into one.
+template <int DT>
+__device__ __forceinline__ void mfma2(uint32_t x, uint32_t a, float &c0, float &c1) {
+  if constexpr (DT == MLORA_BF16)
+    asm("{ .reg .b16 xl, xh, al, ah; mov.b32 {xl, xh}, %2; mov.b32 {al, ah}, %3;\n"
+        " fma.rn.f32.bf16 %0, xl, al, %0; fma.rn.f32.bf16 %1, xh, ah, %1; }"
+        : "+f"(c0), "+f"(c1) : "r"(x), "r"(a));
+  else
+    asm("{ .reg .b16 xl, xh, al, ah; mov.b32 {xl, xh}, %2; mov.b32 {al, ah}, %3;\n"
+        " fma.rn.f32.f16 %0, xl, al, %0; fma.rn.f32.f16 %1, xh, ah, %1; }"
+        : "+f"(c0), "+f"(c1) : "r"(x), "r"(a));
+}
+template <int DT>
+__device__ __forceinline__ void mfma1(uint32_t x, uint32_t a, float &c) {
+  if constexpr (DT == MLORA_BF16)
+    asm("{ .reg .b16 xl, xh, al, ah; mov.b32 {xl, xh}, %1; mov.b32 {al, ah}, %2;\n"
+        " fma.rn.f32.bf16 %0, xl, al, %0; fma.rn.f32.bf16 %0, xh, ah, %0; }"
+        : "+f"(c) : "r"(x), "r"(a));
+  else
+    asm("{ .reg .b16 xl, xh, al, ah; mov.b32 {xl, xh}, %1; mov.b32 {al, ah}, %2;\n"
+        " fma.rn.f32.f16 %0, xl, al, %0; fma.rn.f32.f16 %0, xh, ah, %0; }"
+        : "+f"(c) : "r"(x), "r"(a));
+}
+// Eight products of chunk xv with chunk av (8 packed elements each) into the chains c0, c1.
+template <int DT>
+__device__ __forceinline__ void mfma8(const uint4 &xv, const uint4 &av, float &c0, float &c1) {
+  mfma2<DT>(xv.x, av.x, c0, c1);
+  mfma2<DT>(xv.y, av.y, c0, c1);
+  mfma2<DT>(xv.z, av.z, c0, c1);
+  mfma2<DT>(xv.w, av.w, c0, c1);
+}
+
 template <int DT>
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   uint4 u;

@@ -423,7 +423,9 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
         for (int j = lane; j < rank; j += 32)
           bulk_g2s_hint(bs + j * p.nb, b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2, bbar,
                         evict_first);
-      } else {
+      } else if (!(x_bulk && RT == 1 && k_end - k_begin > KB)) {
+        // (a tile that loops over several passes of A prefetches its B rows at its last pass:
+        // issued now, they would queue ahead of the later passes' A rows)
         for (int j = lane; j < rank; j += 32)
           prefetch_l2(b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2);
       }
@@ -461,65 +463,31 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       for (int jj = 0; jj < JPW; ++jj) acc[i][jj] = 0.f;
 
     if (x_bulk && k_end - k_begin <= KB) {
-      // One row, one pass: each lane reads its x chunks from shared memory, unpacks each once
-      // for all its rank rows and accumulates pairs of products with the paired fp32 FMA (two
-      // independent chains per rank row when a warp has at most 2 rank rows).
+      // One pass: each lane reads its x chunks from shared memory and meets them with its A
+      // chunks in mixed-precision FMAs (16-bit operands, fp32 sums; no unpacking), two chains
+      // per (row, rank row). No guards: A is zero outside the slice and the rank, x is zero in
+      // rows past nr and past the slice, so every chunk and row runs unconditionally.
       const int ok = mbar_wait(ibar, 0) ? 1 : 0;
       timed_out = __syncthreads_or(!ok);
-      if (!timed_out && RT > 1) {
-        // Several rows: A is unpacked once per chunk for a pair of rank rows, then every row's x
-        // chunk meets both; no guards (A is zero outside the slice and the rank, x is zero in
-        // rows past nr and past the slice).
-        constexpr int JG = JPW < 2 ? JPW : 2;
+      if (!timed_out) {
+        float c0[RT][JPW], c1[RT][JPW];
 #pragma unroll
-        for (int jg = 0; jg < JPW; jg += JG) {
+        for (int i = 0; i < RT; ++i)
 #pragma unroll
-          for (int u = 0; u < UK; ++u) {
-            float af[JG][8];
-#pragma unroll
-            for (int q = 0; q < JG; ++q) unpack8<DT>(a[jg + q][u], af[q]);
-#pragma unroll
-            for (int i = 0; i < RT; ++i) {
-              float xf[8];
-              unpack8<DT>(*reinterpret_cast<const uint4 *>(xs + i * XW + (lane + 32 * u) * 8), xf);
-#pragma unroll
-              for (int q = 0; q < JG; ++q) {
-                float t = acc[i][jg + q];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) t = fmaf(xf[e], af[q][e], t);
-                acc[i][jg + q] = t;
-              }
-            }
-          }
-        }
-      } else if (!timed_out) {
-        // No guards: A is zero outside the slice and the rank, x is zero past the slice, so
-        // every chunk and rank row of the pass runs unconditionally (straight-line code).
-        constexpr int CH = JPW <= 2 ? 2 : 1;
-        float2 acc2[JPW][CH];
-#pragma unroll
-        for (int jj = 0; jj < JPW; ++jj)
-#pragma unroll
-          for (int h = 0; h < CH; ++h) acc2[jj][h] = make_float2(0.f, 0.f);
+          for (int jj = 0; jj < JPW; ++jj) c0[i][jj] = c1[i][jj] = 0.f;
 #pragma unroll
         for (int u = 0; u < UK; ++u) {
-          float2 x2[4];
-          unpack8x2<DT>(*reinterpret_cast<const uint4 *>(xs + (lane + 32 * u) * 8), x2);
 #pragma unroll
-          for (int jj = 0; jj < JPW; ++jj) {
-            float2 a2[4];
-            unpack8x2<DT>(a[jj][u], a2);
+          for (int i = 0; i < RT; ++i) {
+            const uint4 xv = *reinterpret_cast<const uint4 *>(xs + i * XW + (lane + 32 * u) * 8);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc2[jj][e % CH] = __ffma2_rn(x2[e], a2[e], acc2[jj][e % CH]);
+            for (int jj = 0; jj < JPW; ++jj) mfma8<DT>(xv, a[jj][u], c0[i][jj], c1[i][jj]);
           }
         }
 #pragma unroll
-        for (int jj = 0; jj < JPW; ++jj) {
-          float2 t2 = acc2[jj][0];
+        for (int i = 0; i < RT; ++i)
 #pragma unroll
-          for (int h = 1; h < CH; ++h) t2 = make_float2(t2.x + acc2[jj][h].x, t2.y + acc2[jj][h].y);
-          acc[0][jj] = t2.x + t2.y;
-        }
+          for (int jj = 0; jj < JPW; ++jj) acc[i][jj] = c0[i][jj] + c1[i][jj];
       }
     } else if (x_bulk && RT == 1) {
       // The x slice is in shared memory; A comes in passes of KB elements (the first loaded into
@@ -527,39 +495,24 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       // guards: A is zero outside the slice and the rank, x is zero past the slice and nr.
       const int ok = mbar_wait(ibar, 0) ? 1 : 0;
       timed_out = __syncthreads_or(!ok);
-      constexpr int CH = JPW <= 2 ? 2 : 1;
-      float2 acc2[JPW][CH];  // one-row tiles: pairs of products, CH independent chains per rank row
+      float c0[JPW], c1[JPW];  // two chains per rank row, across the passes
 #pragma unroll
-      for (int jj = 0; jj < JPW; ++jj)
-#pragma unroll
-        for (int h = 0; h < CH; ++h) acc2[jj][h] = make_float2(0.f, 0.f);
+      for (int jj = 0; jj < JPW; ++jj) c0[jj] = c1[jj] = 0.f;
       for (int pass = 0; !timed_out && pass * KB < k_end - k_begin; ++pass) {
         if (pass > 0) load_a(k_begin + pass * KB);
         const uint16_t *xp = xs + pass * KB;
-          // One row: each lane unpacks its x chunk once for all its rank rows and accumulates
-          // pairs of products with the paired fp32 FMA.
+        if (!b_staged && do_expand && n_end > n_begin && (pass + 1) * KB >= k_end - k_begin)
+          for (int j = tid; j < rank; j += NTHREADS)
+            prefetch_l2(b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2);
 #pragma unroll
-          for (int u = 0; u < UK; ++u) {
-            float2 x2[4];
-            unpack8x2<DT>(*reinterpret_cast<const uint4 *>(xp + (lane + 32 * u) * 8), x2);
+        for (int u = 0; u < UK; ++u) {
+          const uint4 xv = *reinterpret_cast<const uint4 *>(xp + (lane + 32 * u) * 8);
 #pragma unroll
-            for (int jj = 0; jj < JPW; ++jj) {
-              float2 a2[4];
-              unpack8x2<DT>(a[jj][u], a2);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) acc2[jj][e % CH] = __ffma2_rn(x2[e], a2[e], acc2[jj][e % CH]);
-            }
-          }
-      }
-      {
-#pragma unroll
-        for (int jj = 0; jj < JPW; ++jj) {
-          float2 t2 = acc2[jj][0];
-#pragma unroll
-          for (int h = 1; h < CH; ++h) t2 = make_float2(t2.x + acc2[jj][h].x, t2.y + acc2[jj][h].y);
-          acc[0][jj] = t2.x + t2.y;
+          for (int jj = 0; jj < JPW; ++jj) mfma8<DT>(xv, a[jj][u], c0[jj], c1[jj]);
         }
       }
+#pragma unroll
+      for (int jj = 0; jj < JPW; ++jj) acc[0][jj] = c0[jj] + c1[jj];
     } else if (do_shrink) {
       for (int kb0 = k_begin; kb0 < k_end; kb0 += KB) {
         const int n8 = min(KB, k_end - kb0) >> 3;
@@ -701,7 +654,9 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc2[e] = __ffma2_rn(v2, b2[e], acc2[e]);
         };
-        constexpr int UB = 8;  // B rows in flight per thread when they come from global memory
+        // B rows in flight per thread when they come from global memory: 16 above rank 16 (half
+        // the round trips to L2; the A registers are free by now)
+        constexpr int UB = VREG ? 8 : 16;
         if constexpr (VREG) {
           if (b_staged && rank == RV) {  // every rank row present: straight-line, no guards
 #pragma unroll
