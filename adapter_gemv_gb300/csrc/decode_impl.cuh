@@ -22,8 +22,9 @@
 //     the wait one thread bulk-copies the tile's x rows (and y rows, when they fit) into shared
 //     memory. Later passes of A, and B rows that do not fit, come from L2, prefetched there.
 //   * Arithmetic runs on data already on chip, as straight-line code without per-chunk or
-//     per-row guards (the staged operands are zero where they lie outside the tile), with the
-//     paired fp32 FMA.
+//     per-row guards (the staged operands are zero where they lie outside the tile). The shrink
+//     meets packed 16-bit x and A directly in mixed-precision FMAs (fp32 sums, no unpacking);
+//     the expand, whose v is fp32, uses the paired fp32 FMA.
 //   * Programmatic dependent launch (when the caller enables it): a kernel lets the next one in
 //     the stream start at once. Before griddepcontrol.wait a CTA only reads what no kernel of
 //     this library writes (the rows' metadata, the pool, the page tables); x, y and v, which the
