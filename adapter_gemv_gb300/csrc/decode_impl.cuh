@@ -292,6 +292,13 @@ struct Pass {
   static constexpr int KB = 256 * UK;
 };
 
+// A layout of the same 16 A registers with JN (<= JPW) rank rows per warp: a tile whose rank
+// needs fewer rows than the pool's maximum covers 16 / JN chunks of d_in per lane and pass.
+template <int JN>
+struct Rows {
+  static constexpr int value = JN;
+};
+
 template <int DT, int MODE, int RT, int JPW>
 __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -356,6 +363,36 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   const bool x_bulk = do_shrink && k_end > k_begin && k_end - k_begin <= XW;
   const bool y_bulk = do_expand && p.ny > 0 && n_end > n_begin;
   const uint64_t evict_first = policy_evict_first();
+  // Rank rows per warp of this tile's A layout. A one-row tile whose x slice sits in shared
+  // memory and needs several passes of A takes the fewest rows its rank allows (a power of
+  // two), so the same registers cover more of d_in per pass -- as long as every pass stays
+  // inside the XW elements of xs (guard-free reads). Otherwise the pool's JPW.
+  int jn = JPW;
+  if constexpr (JPW >= 4) {
+    if (x_bulk && RT == 1 && k_end - k_begin > KB) {
+      const int slice = k_end - k_begin;
+#pragma unroll
+      for (int q = JPW / 2; q >= 1; q >>= 1) {
+        const int kbq = 256 * (16 / q);
+        if (q * NWARPS >= rank && (slice + kbq - 1) / kbq * kbq <= XW) jn = q;
+      }
+    }
+  }
+  const int kbn = 256 * (16 / jn);  // K elements per pass of A in this layout
+  // Runs f(Rows<jn>) with jn a compile-time constant (one copy of f per layout in use).
+  auto with_rows = [&](auto f) {
+    if constexpr (JPW >= 4) {
+      if (jn == 1) return f(Rows<1>{});
+      if (jn == 2) return f(Rows<2>{});
+    }
+    if constexpr (JPW >= 8) {
+      if (jn == 4) return f(Rows<4>{});
+    }
+    if constexpr (JPW >= 16) {
+      if (jn == 8) return f(Rows<8>{});
+    }
+    return f(Rows<JPW>{});
+  };
 
   // Everything that no kernel writes -- the adapter rows -- is requested before waiting for the
   // previous kernel: the first pass of A into registers, this CTA's B rows into shared memory.
@@ -368,9 +405,9 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       for (int i = lane; i < nr; i += 32)
         prefetch_l2(pr.y + (int64_t)(row0 + i) * pr.ldy + n_begin, (uint32_t)(n_end - n_begin) * 2);
     }
-    if (do_shrink && k_end - k_begin > KB)
+    if (do_shrink && k_end - k_begin > kbn)
       for (int j = lane; j < rank; j += 32)
-        prefetch_l2(a_row(pl, s, pr.layer, j) + k_begin + KB, (uint32_t)(k_end - k_begin - KB) * 2);
+        prefetch_l2(a_row(pl, s, pr.layer, j) + k_begin + kbn, (uint32_t)(k_end - k_begin - kbn) * 2);
     if (clustered && lane == 0) mbar_arrive_expect_tx(xbar, (uint32_t)(cs * nr * rank * 4));
   }
   // Prefetch hint: the adapter rows the next call will read for this tile's slot, shared out
@@ -401,22 +438,25 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
     }
   }
 
+  // A registers: in the Rows<JN> layout, register i = jj * (16 / JN) + u holds chunk
+  // c8 = lane + 32 u of rank row j = warp + NWARPS jj (a[i / UK][i % UK]; JN = JPW is [jj][u]).
   uint4 a[JPW][UK];
-  auto load_a = [&](int kb0) {
-    const int n8 = min(KB, k_end - kb0) >> 3;
+  auto load_a = [&](auto rows, int kb0) {
+    constexpr int JN = decltype(rows)::value, UKN = 16 / JN;
+    const int n8 = min(256 * UKN, k_end - kb0) >> 3;
 #pragma unroll
-    for (int jj = 0; jj < JPW; ++jj) {
+    for (int jj = 0; jj < JN; ++jj) {
       const int j = warp + jj * NWARPS;
 #pragma unroll
-      for (int u = 0; u < UK; ++u) {
-        const int c8 = lane + 32 * u;
+      for (int u = 0; u < UKN; ++u) {
+        const int c8 = lane + 32 * u, i = jj * UKN + u;
         // zero outside the slice and the rank: the one-row loop below then needs no guards
-        a[jj][u] = (j < rank && c8 < n8) ? ldg_stream(a_row(pl, s, pr.layer, j) + kb0 + c8 * 8, evict_first)
-                                         : make_uint4(0u, 0u, 0u, 0u);
+        a[i / UK][i % UK] = (j < rank && c8 < n8) ? ldg_stream(a_row(pl, s, pr.layer, j) + kb0 + c8 * 8, evict_first)
+                                                  : make_uint4(0u, 0u, 0u, 0u);
       }
     }
   };
-  if (do_shrink) load_a(k_begin);
+  if (do_shrink) with_rows([&](auto rows) { load_a(rows, k_begin); });
   if (active && warp == 0 && do_expand && n_end > n_begin) {
       if (b_staged) {
         if (lane == 0) mbar_arrive_expect_tx(bbar, (uint32_t)(rank * (n_end - n_begin) * 2));
@@ -424,7 +464,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
         for (int j = lane; j < rank; j += 32)
           bulk_g2s_hint(bs + j * p.nb, b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2, bbar,
                         evict_first);
-      } else if (!(x_bulk && RT == 1 && k_end - k_begin > KB)) {
+      } else if (!(x_bulk && RT == 1 && k_end - k_begin > kbn)) {
         // (a tile that loops over several passes of A prefetches its B rows at its last pass:
         // issued now, they would queue ahead of the later passes' A rows)
         for (int j = lane; j < rank; j += 32)
@@ -499,25 +539,34 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       float c0[JPW], c1[JPW];  // two chains per rank row, across the passes
 #pragma unroll
       for (int jj = 0; jj < JPW; ++jj) c0[jj] = c1[jj] = 0.f;
-      for (int pass = 0; !timed_out && pass * KB < k_end - k_begin; ++pass) {
-        if (pass > 0) load_a(k_begin + pass * KB);
-        const uint16_t *xp = xs + pass * KB;
-        if (!b_staged && do_expand && n_end > n_begin && (pass + 1) * KB >= k_end - k_begin)
-          for (int j = tid; j < rank; j += NTHREADS)
-            prefetch_l2(b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2);
+      with_rows([&](auto rows) {
+        constexpr int JN = decltype(rows)::value, UKN = 16 / JN, KBN = 256 * UKN;
+        for (int pass = 0; !timed_out && pass * KBN < k_end - k_begin; ++pass) {
+          if (pass > 0) load_a(rows, k_begin + pass * KBN);
+          const uint16_t *xp = xs + pass * KBN;  // pass < ceil(slice / KBN), so xp + KBN <= xs + XW
+          // B rows of a tile with several passes are prefetched at its last one (a one-pass tile
+          // prefetched them before the wait)
+          if (pass > 0 && !b_staged && do_expand && n_end > n_begin && (pass + 1) * KBN >= k_end - k_begin)
+            for (int j = tid; j < rank; j += NTHREADS)
+              prefetch_l2(b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2);
 #pragma unroll
-        for (int u = 0; u < UK; ++u) {
-          const uint4 xv = *reinterpret_cast<const uint4 *>(xp + (lane + 32 * u) * 8);
+          for (int u = 0; u < UKN; ++u) {
+            const uint4 xv = *reinterpret_cast<const uint4 *>(xp + (lane + 32 * u) * 8);
 #pragma unroll
-          for (int jj = 0; jj < JPW; ++jj) mfma8<DT>(xv, a[jj][u], c0[jj], c1[jj]);
+            for (int jj = 0; jj < JN; ++jj) {
+              const int i = jj * UKN + u;
+              mfma8<DT>(xv, a[i / UK][i % UK], c0[jj], c1[jj]);
+            }
+          }
         }
-      }
+      });
+      // rank rows jj >= JN of this layout lie past the rank: their sums stay zero
 #pragma unroll
       for (int jj = 0; jj < JPW; ++jj) acc[0][jj] = c0[jj] + c1[jj];
     } else if (do_shrink) {
       for (int kb0 = k_begin; kb0 < k_end; kb0 += KB) {
         const int n8 = min(KB, k_end - kb0) >> 3;
-        if (kb0 != k_begin) load_a(kb0);
+        if (kb0 != k_begin) load_a(Rows<JPW>{}, kb0);
         // x rows of this pass -> shared memory (read by every warp)
         for (int e = tid; e < nr * n8; e += NTHREADS) {
           const int i = e / n8, c8 = e % n8;

@@ -119,6 +119,58 @@ def test_fuzz_two_phase_and_fused(dev, shape, seed, form):
     check_op(op, batch, form, g1.y, what="fused")
 
 
+
+# One-row tiles whose d_in slice spans several passes of A hold as few rank rows per warp as
+# their rank allows (1, 2, 4 or 8 of a warp's 8, 16 ways), and use the freed registers for more
+# of d_in per pass, as long as whole passes stay inside the x slice in shared memory. The
+# shapes are chosen, against the launcher's split rule, so that single calls produce such tiles:
+#   r_max 64,  d_in 6000, M 200: 6 CTAs per row, slices of 1000, x slice 1024 wide; ranks <= 32
+#     take one pass of 1024, ranks 33..64 two passes of 512;
+#   r_max 128, d_in 7168, M 160: 7 CTAs per row, slices of 1024; ranks <= 32 one pass, ranks
+#     33..64 two passes, ranks above 64 four passes of 256.
+# The slots' ranks sit on both sides of every layout boundary; every seventh row has no adapter.
+RANK_LAYOUT_CASES = [
+    # r_max, d_in, d_out, M, ranks of the slots
+    (64, 6000, 1000, 200, [1, 8, 9, 16, 17, 32, 33, 64]),
+    (128, 7168, 520, 160, [1, 8, 9, 32, 33, 64, 65, 128]),
+]
+
+
+@pytest.mark.parametrize("paged", [False, True], ids=["stacked", "paged"])
+@pytest.mark.parametrize("case", RANK_LAYOUT_CASES, ids=lambda c: f"r{c[0]}-{c[1]}x{c[2]}-M{c[3]}")
+@pytest.mark.parametrize("form", ["sgmv", "bgmv"])
+def test_rank_aware_a_layouts(dev, case, paged, form):
+    r_max, d_in, d_out, M, slot_ranks = case
+    rng = np.random.default_rng(7 + r_max)
+    g = W.generator(7 + r_max, dev)
+    ranks = np.asarray(slot_ranks, np.int32)
+    kw = dict(num_slots=len(ranks), num_layers=1, r_max=r_max, d_in=d_in, d_out=d_out, dtype=torch.bfloat16,
+              gen=g, device=dev, ranks=ranks)
+    pool = W.paged_pool(rng=rng, **kw) if paged else W.stacked_pool(**kw)
+    slots = (np.arange(M) % len(ranks)).astype(np.int32)
+    slots[::7] = -1
+    batch = W.batch_from_segments(np.ones(M, np.int64), slots).to(dev)  # one row per segment
+    x = W.normal((M, d_in), 1.0, torch.bfloat16, g, dev)
+    y = W.uniform((M, d_out), -1, 1, torch.bfloat16, g, dev)
+    op = W.Op("rank_layouts", pool, 0, x, y)
+    h = m.make_pool(pool)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    g2, g1 = Guarded(op.y, r_max), Guarded(op.y, r_max)
+    if form == "sgmv":
+        m.lora_sgmv_shrink(g2.v, x, h, batch.seg_offsets, batch.seg_slot, 0, st)
+        m.lora_sgmv_expand(g2.y, g2.v, h, batch.seg_offsets, batch.seg_slot, 0, st)
+        m.lora_sgmv(g1.y, x, h, batch.seg_offsets, batch.seg_slot, 0, g1.v, st)
+    else:
+        m.lora_bgmv_shrink(g2.v, x, h, batch.row_slot, 0, st)
+        m.lora_bgmv_expand(g2.y, g2.v, h, batch.row_slot, 0, st)
+        m.lora_bgmv(g1.y, x, h, batch.row_slot, 0, g1.v, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    g2.check(True)
+    g1.check(False)
+    check_op(op, batch, form, g2.y, g2.v, what="two-phase")
+    check_op(op, batch, form, g1.y, what="fused")
+
 def test_status_contract_matches_oracle(dev):
     """Bad offsets / slots / ranks / pages: same status bits as the oracle, affected rows
     untouched bit for bit, all other rows correct."""
