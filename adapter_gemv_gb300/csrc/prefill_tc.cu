@@ -290,9 +290,10 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
 // rows) and the block's columns 32 (w / 4) .. +31; warps 0-3 also build V, one row per thread;
 // warp 8 lane 0 loads (TMA) the y tile and B rows of each 64-column block into a ring of
 // buffers; warp 9 lane 0 issues the MMAs into one of two TMEM accumulators, so a block's MMA
-// overlaps the previous block's epilogue.
+// overlaps the previous block's epilogue; warp 10 lane 0 stores each finished y tile (TMA) and
+// frees its buffer once the store has read it, so the epilogue goes on to the next block at once.
 constexpr int EXP_EPI_WARPS = 8;
-constexpr int EXP_THREADS = (EXP_EPI_WARPS + 2) * 32;
+constexpr int EXP_THREADS = (EXP_EPI_WARPS + 3) * 32;
 
 // Shared memory: V hi / lo, then EBUF pipeline buffers, each with the y tile of one 64-column
 // block (128 rows x 128 B) followed by its B rows (one MN atom: rpad K rows x 128 B).
@@ -317,12 +318,8 @@ struct ExpandSmem {
 
 constexpr int EBN = 64;  // expand: columns per pipeline block (MMA N)
 
-// Named barrier for the epilogue warps only (id 1; id 0 is __syncthreads).
-__device__ __forceinline__ void epi_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(EXP_EPI_WARPS * 32) : "memory");
-}
-
-// The same barrier, returning whether any epilogue thread passed a nonzero value.
+// Named barrier for the epilogue warps only (id 1; id 0 is __syncthreads), returning whether
+// any epilogue thread passed a nonzero value.
 __device__ __forceinline__ int epi_sync_or(int v) {
   int r;
   asm volatile(
@@ -347,7 +344,8 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
   uint64_t *accfull = empty + MAX_EBUF;   // [2] accumulator a holds a finished block
   uint64_t *accempty = accfull + 2;   // [2] the epilogue has read accumulator a
   uint64_t *mmadone = accempty + 2;   // every MMA this CTA issued has completed
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mmadone + 1);
+  uint64_t *ystaged = mmadone + 1;    // [EBUF] the epilogue has finished the buffer's y tile
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ystaged + MAX_EBUF);
   int32_t *flags = reinterpret_cast<int32_t *>(tmem_slot + 1);  // [0] = timed out
   TcTile *ti = reinterpret_cast<TcTile *>(smem + L.bar_off + 256);
   int32_t *scan = reinterpret_cast<int32_t *>(smem + L.bar_off + 1024);
@@ -362,6 +360,7 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
     for (int b = 0; b < EBUF; ++b) {
       mbar_init(&full[b], 1);
       mbar_init(&empty[b], 1);
+      mbar_init(&ystaged[b], EXP_EPI_WARPS * 32);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&accfull[a], 1);
@@ -488,6 +487,25 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
       (void)mbar_wait(mmadone, 0, 100000000ull);
     }
     __syncwarp();
+  } else if (active && warp == EXP_EPI_WARPS + 2) {
+    // ---- store (one lane): each finished y tile goes out by TMA; its buffer is freed once the
+    // store has read it (a partial tile was written by the epilogue with plain stores)
+    if (lane == 0) {
+      for (int i = 0; i < nblk; ++i) {
+        if (!mbar_wait(&ystaged[i % EBUF], (uint32_t)(i / EBUF) & 1u)) {
+          flags[0] = 1;
+          break;
+        }
+        if (full_tile) {
+          tc::tma_store_2d(&tm_y, (nb_begin + i) * EBN, row0, buf(i));  // columns past d_out are clipped
+          tc::bulk_commit_group();
+          tc::bulk_wait_group_read<0>();
+        }
+        mbar_arrive(&empty[i % EBUF]);
+      }
+      tc::bulk_wait_group_all();  // stores complete before the shared memory goes away
+    }
+    __syncwarp();
   } else if (active) {
     // ---- epilogue: row m of the block's y tile += scale * D (this warp's 32 columns), rounded once
     const int m = (warp & 3) * 32 + lane, half = warp >> 2;
@@ -524,18 +542,9 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
           *reinterpret_cast<uint4 *>(p.y + (int64_t)(row0 + m) * p.ldy + nb * EBN + ch * 8) = pack8<DT>(yf);
         }
       }
-      tc::fence_proxy_async();
-      epi_sync();
-      if (tid == 0) {
-        if (full_tile) tc::tma_store_2d(&tm_y, nb * EBN, row0, ys);  // columns past d_out are clipped
-        tc::bulk_commit_group();
-        // once this block's store has read its tile (a short wait: shared memory to L2), the
-        // buffer may be refilled
-        tc::bulk_wait_group_read<0>();
-        mbar_arrive(&empty[i % EBUF]);
-      }
+      tc::fence_proxy_async();          // this thread's y writes -> visible to the TMA store
+      mbar_arrive(&ystaged[i % EBUF]);  // the store warp takes the tile from here
     }
-    if (tid == 0) tc::bulk_wait_group_all();  // stores complete before the shared memory goes away
   }
   __syncthreads();
   if (active && flags[0] && tid == 0) report(p.status, MLORA_STATUS_TIMEOUT);
