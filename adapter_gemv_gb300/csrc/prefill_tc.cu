@@ -318,18 +318,6 @@ struct ExpandSmem {
 
 constexpr int EBN = 64;  // expand: columns per pipeline block (MMA N)
 
-// Named barrier for the epilogue warps only (id 1; id 0 is __syncthreads), returning whether
-// any epilogue thread passed a nonzero value.
-__device__ __forceinline__ int epi_sync_or(int v) {
-  int r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 q, %1, 0;\n\tbar.red.or.pred p, 1, %2, q;\n\tselp.s32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(v), "n"(EXP_EPI_WARPS * 32)
-      : "memory");
-  return r;
-}
-
 template <int DT>
 __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_constant__ CUtensorMap tm_b,
                                                                 const __grid_constant__ CUtensorMap tm_y,
@@ -515,8 +503,11 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
       uint8_t *ys = buf(i);
       int ok = mbar_wait(&accfull[a], (uint32_t)(i >> 1) & 1u) ? 1 : 0;
       ok &= mbar_wait(&full[i % EBUF], (uint32_t)(i / EBUF) & 1u) ? 1 : 0;  // the y tile is visible
-      if (!ok) flags[0] = 1;
-      if (epi_sync_or(!ok || flags[0])) break;  // the same decision in every epilogue thread
+      if (!ok) {  // no barrier across the epilogue warps: each goes its own pace; a thread that
+                  // gives up leaves its later arrivals out, so the other roles' bounded waits end too
+        flags[0] = 1;
+        break;
+      }
       tc::tc_fence_after();
       float d[EBN / 2];
 #pragma unroll
