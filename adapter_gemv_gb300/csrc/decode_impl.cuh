@@ -363,12 +363,14 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   const bool x_bulk = do_shrink && k_end > k_begin && k_end - k_begin <= XW;
   const bool y_bulk = do_expand && p.ny > 0 && n_end > n_begin;
   const uint64_t evict_first = policy_evict_first();
-  // Rank rows per warp of this tile's A layout. A one-row tile whose x slice sits in shared
-  // memory and needs several passes of A takes the fewest rows its rank allows (a power of
-  // two), so the same registers cover more of d_in per pass -- as long as every pass stays
-  // inside the XW elements of xs (guard-free reads). Otherwise the pool's JPW.
+  // Rank rows per warp of this tile's A layout. A one-row tile of the fused kernel whose x slice
+  // sits in shared memory and needs several passes of A takes the fewest rows its rank allows (a
+  // power of two), so the same registers cover more of d_in per pass -- as long as every pass
+  // stays inside the XW elements of xs (guard-free reads). Otherwise the pool's JPW. (The
+  // shrink-only kernel keeps JPW: with the smaller layouts it measured slower, 55.6 -> 57.0 us on
+  // a 70B q_proj batch with ranks 8..64, and the shrink + expand pair 92.5 -> 97.5 us.)
   int jn = JPW;
-  if constexpr (JPW >= 4) {
+  if constexpr (JPW >= 4 && MODE == MODE_FUSED) {
     if (x_bulk && RT == 1 && k_end - k_begin > KB) {
       const int slice = k_end - k_begin;
 #pragma unroll
