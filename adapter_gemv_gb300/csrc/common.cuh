@@ -54,10 +54,10 @@ __device__ __forceinline__ void unpack8x2(const uint4 &u, float2 (&f)[4]) {
   f[3] = make_float2(Elem<DT>::lo(u.w), Elem<DT>::hi(u.w));
 }
 
-// Mixed-precision FMA on packed 16-bit pairs: the products of the low halves and of the high
-// halves of x and a are added in fp32 (the product of two bf16 or two fp16 values is exact in
-// fp32, so this equals unpacking both and using the fp32 FMA), one instruction per product and
-// no unpacking. mfma2: into two accumulators; mfma1: both into one.
+// Mixed-precision FMA on packed 16-bit pairs: c0 += lo(x) * lo(a), c1 += hi(x) * hi(a), with
+// 16-bit operands and fp32 accumulators, one instruction per product and no unpacking. Like the
+// fp32 FMA on the unpacked operands, each computes x * a + c and rounds once, so the results
+// are the same.
 template <int DT>
 __device__ __forceinline__ void mfma2(uint32_t x, uint32_t a, float &c0, float &c1) {
   if constexpr (DT == MLORA_BF16)
@@ -68,17 +68,6 @@ __device__ __forceinline__ void mfma2(uint32_t x, uint32_t a, float &c0, float &
     asm("{ .reg .b16 xl, xh, al, ah; mov.b32 {xl, xh}, %2; mov.b32 {al, ah}, %3;\n"
         " fma.rn.f32.f16 %0, xl, al, %0; fma.rn.f32.f16 %1, xh, ah, %1; }"
         : "+f"(c0), "+f"(c1) : "r"(x), "r"(a));
-}
-template <int DT>
-__device__ __forceinline__ void mfma1(uint32_t x, uint32_t a, float &c) {
-  if constexpr (DT == MLORA_BF16)
-    asm("{ .reg .b16 xl, xh, al, ah; mov.b32 {xl, xh}, %1; mov.b32 {al, ah}, %2;\n"
-        " fma.rn.f32.bf16 %0, xl, al, %0; fma.rn.f32.bf16 %0, xh, ah, %0; }"
-        : "+f"(c) : "r"(x), "r"(a));
-  else
-    asm("{ .reg .b16 xl, xh, al, ah; mov.b32 {xl, xh}, %1; mov.b32 {al, ah}, %2;\n"
-        " fma.rn.f32.f16 %0, xl, al, %0; fma.rn.f32.f16 %0, xh, ah, %0; }"
-        : "+f"(c) : "r"(x), "r"(a));
 }
 // Eight products of chunk xv with chunk av (8 packed elements each) into the chains c0, c1.
 template <int DT>
