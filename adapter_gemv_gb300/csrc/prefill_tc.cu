@@ -390,13 +390,17 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
   if (active && warp == EXP_EPI_WARPS && lane == 0)
     for (; issued < nblk && issued < EBUF; ++issued) issue(issued);
 
-  // V hi / lo in the K-major 128-byte-swizzle layout: epilogue thread m owns row m
+  // V hi / lo in the K-major 128-byte-swizzle layout: epilogue thread m owns row m. fp16 rows
+  // are stored as v * 2^-vexp[m], with vexp[m] chosen so that the row's largest |v| stays below
+  // 2^14 (fp16 overflows at 65504, where bf16 and the fp32 v do not); the epilogue of row m
+  // multiplies its sums by 2^vexp[m]. The scaling is exact (a power of two); bf16 rows are not
+  // scaled.
+  int32_t *vexp = reinterpret_cast<int32_t *>(smem + L.bar_off + 512);  // [BM]
   if (active && warp < 4) {
     const int m = tid;
     const float *vrow = p.v + (int64_t)(row0 + (m < nr ? m : 0)) * p.r_max;
     const bool vec = ((p.r_max & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.v) & 15) == 0);
-    for (int c8 = 0; c8 < katoms * 8; ++c8) {  // 16-byte chunks of 8 K elements
-      float f[8], hi[8], lo[8];
+    auto load8 = [&](int c8, float (&f)[8]) {  // 8 K elements of row m, zero past the rank and nr
       if (m >= nr) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) f[e] = 0.f;
@@ -410,6 +414,31 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
           const int j = c8 * 8 + e;
           f[e] = (j < rank) ? vrow[j] : 0.f;
         }
+      }
+    };
+    float rs = 1.f;  // 2^-vexp[m]
+    if constexpr (DT == MLORA_FP16) {
+      float amax = 0.f;
+      for (int c8 = 0; c8 < katoms * 8; ++c8) {
+        float f[8];
+        load8(c8, f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+      }
+      int e2 = 0;
+      (void)frexpf(amax, &e2);  // amax = mant * 2^e2, mant in [0.5, 1); e2 <= 128
+      const int s = e2 > 14 ? e2 - 14 : 0;
+      vexp[m] = s;
+      rs = __int_as_float((127 - s) << 23);
+    } else {
+      vexp[m] = 0;
+    }
+    for (int c8 = 0; c8 < katoms * 8; ++c8) {  // 16-byte chunks of 8 K elements
+      float f[8], hi[8], lo[8];
+      load8(c8, f);
+      if constexpr (DT == MLORA_FP16) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] *= rs;
       }
       const uint4 h = pack8<DT>(f);
       unpack8<DT>(h, hi);
@@ -497,6 +526,8 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
   } else if (active) {
     // ---- epilogue: row m of the block's y tile += scale * D (this warp's 32 columns), rounded once
     const int m = (warp & 3) * 32 + lane, half = warp >> 2;
+    // fp16 V row m was stored scaled by 2^-vexp[m]: its sums carry the factor back (exact)
+    const float rscale = DT == MLORA_FP16 ? scale * __int_as_float((127 + vexp[m]) << 23) : scale;
     int i = 0;
     for (; i < nblk; ++i) {
       const int a = i & 1, nb = nb_begin + i;
@@ -526,7 +557,7 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
         float yf[8];
         unpack8<DT>(*cell, yf);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) yf[e] = fmaf(scale, d[cq * 8 + e], yf[e]);
+        for (int e = 0; e < 8; ++e) yf[e] = fmaf(rscale, d[cq * 8 + e], yf[e]);
         if (full_tile) {
           *cell = pack8<DT>(yf);
         } else if (m < nr && nb * EBN + ch * 8 < p.d_out) {
@@ -601,7 +632,8 @@ cudaError_t set_smem(K kern, size_t smem) {
 constexpr int TC_MIN_ROWS = kTcMinRows;
 
 bool tc_eligible(const PoolDev &pool, int num_rows, int nseg) {
-  return pool.kind == MLORA_POOL_STACKED && pool.dtype == MLORA_BF16 && pool.r_max <= 128 && num_rows >= BM &&
+  return pool.kind == MLORA_POOL_STACKED && (pool.dtype == MLORA_BF16 || pool.dtype == MLORA_FP16) &&
+         pool.r_max <= 128 && num_rows >= BM &&
          (int64_t)num_rows >= (int64_t)64 * (nseg > 0 ? nseg : 1) && encoder() != nullptr;
 }
 
@@ -615,7 +647,7 @@ cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stre
   const int kb_total = (pl.d_in + SKA * BK - 1) / (SKA * BK);
   p.stages = ShrinkSmem::make(p.rpad).stages;
   const size_t smem = ShrinkSmem::make(p.rpad, p.stages).total;
-  auto kern = tc_shrink_kernel<MLORA_BF16>;
+  auto kern = pl.dtype == MLORA_BF16 ? tc_shrink_kernel<MLORA_BF16> : tc_shrink_kernel<MLORA_FP16>;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   // K split: as many parts as keep the whole grid resident (one wave)
@@ -666,7 +698,7 @@ cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stre
   if (!encode_2d(&tm_y, pl.dtype, pr.y, pl.d_out, p.M, pr.ldy, BM)) return cudaErrorInvalidValue;
   p.stages = ExpandSmem::make(p.rpad, 0, expand_budget).nbuf;
   const size_t smem = ExpandSmem::make(p.rpad, p.stages).total;
-  auto kern = tc_expand_kernel<MLORA_BF16>;
+  auto kern = pl.dtype == MLORA_BF16 ? tc_expand_kernel<MLORA_BF16> : tc_expand_kernel<MLORA_FP16>;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((p.nblk_total + p.nper - 1) / p.nper, p.tiles, 1);

@@ -1,7 +1,8 @@
 """Tensor-core prefill path against the oracle: long SGMV segments whose full 128-row blocks run
 on tcgen05 kernels and whose tails run on the CUDA-core kernels. Segment lengths around the
 128-row boundary, empty and -1 segments, K and N extents that are not multiples of the tile,
-ranks below the padded rank (padding rows hold NaN), every row compared."""
+ranks below the padded rank (padding rows hold NaN), bf16 and fp16 pools, fp16 shrink results
+beyond the fp16 range, every row compared."""
 import numpy as np
 import pytest
 import torch
@@ -37,34 +38,63 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"r{c[0]}-{c[2]}x{c[3]}-M{sum(c[4])}")
-@pytest.mark.parametrize("mode", ["two_phase", "fused"])
-def test_prefill_tensor_core_path(dev, case, mode):
-    r_max, ranks, d_in, d_out, lens, slots = case
-    g = W.generator(7, dev)
-    pool = W.stacked_pool(num_slots=len(ranks), num_layers=2, r_max=r_max, d_in=d_in, d_out=d_out,
-                          dtype=torch.bfloat16, gen=g, device=dev, ranks=ranks)
-    batch = W.batch_from_segments(lens, slots).to(dev)
+def run_tc(dev, op, batch, mode, r_max):
+    """One op through the tensor-core path (two launches or fused); checks that it ran there."""
     M = batch.M
-    x = W.normal((M, d_in), 1.0, torch.bfloat16, g, dev)
-    y0 = W.uniform((M, d_out), -1, 1, torch.bfloat16, g, dev)
-    op = W.Op("p", pool, 1, x, y0)
-    h = m.make_pool(pool)
+    h = m.make_pool(op.pool)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    y = y0.clone()
+    y = op.y.clone()
     v = new_v(M, r_max, dev)
     before = m.launch_count()
     if mode == "two_phase":
-        m.lora_sgmv_shrink(v, x, h, batch.seg_offsets, batch.seg_slot, 1, st)
-        m.lora_sgmv_expand(y, v, h, batch.seg_offsets, batch.seg_slot, 1, st)
+        m.lora_sgmv_shrink(v, op.x, h, batch.seg_offsets, batch.seg_slot, op.layer, st)
+        m.lora_sgmv_expand(y, v, h, batch.seg_offsets, batch.seg_slot, op.layer, st)
         launches = 4  # tensor-core shrink + tails, tensor-core expand + tails
     else:
-        m.lora_sgmv(y, x, h, batch.seg_offsets, batch.seg_slot, 1, v, st)
+        m.lora_sgmv(y, op.x, h, batch.seg_offsets, batch.seg_slot, op.layer, v, st)
         launches = 3
     torch.cuda.synchronize()
     assert m.launch_count() - before == launches, "the tensor-core path did not run"
     assert st.item() == 0
+    return y, v
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"r{c[0]}-{c[2]}x{c[3]}-M{sum(c[4])}")
+@pytest.mark.parametrize("mode", ["two_phase", "fused"])
+def test_prefill_tensor_core_path(dev, case, mode, dtype):
+    r_max, ranks, d_in, d_out, lens, slots = case
+    g = W.generator(7, dev)
+    pool = W.stacked_pool(num_slots=len(ranks), num_layers=2, r_max=r_max, d_in=d_in, d_out=d_out,
+                          dtype=dtype, gen=g, device=dev, ranks=ranks)
+    batch = W.batch_from_segments(lens, slots).to(dev)
+    M = batch.M
+    x = W.normal((M, d_in), 1.0, dtype, g, dev)
+    y0 = W.uniform((M, d_out), -1, 1, dtype, g, dev)
+    op = W.Op("p", pool, 1, x, y0)
+    y, v = run_tc(dev, op, batch, mode, r_max)
     check_op(op, batch, "sgmv", y, v if mode == "two_phase" else None, what=f"tc {mode}")
+
+
+@pytest.mark.parametrize("mode", ["two_phase", "fused"])
+def test_prefill_fp16_shrink_results_beyond_fp16_range(dev, mode):
+    """fp16 pool whose shrink results v reach past 65504 (x std 4096, A std 8 / sqrt(d_in), so v
+    has std 32768): the tensor-core expand stores each row of V scaled by a power of two and
+    scales the row's sums back, so y still matches the oracle."""
+    d_in, d_out, r = 1024, 512, 32
+    g = W.generator(9, dev)
+    pool = W.stacked_pool(num_slots=2, num_layers=1, r_max=r, d_in=d_in, d_out=d_out, dtype=torch.float16, gen=g,
+                          device=dev, a_var=64.0 / d_in, b_var=1e-4)
+    batch = W.batch_from_segments([256, 130], [0, 1]).to(dev)
+    x = W.normal((batch.M, d_in), 4096.0 ** 2, torch.float16, g, dev)
+    y0 = W.uniform((batch.M, d_out), -1, 1, torch.float16, g, dev)
+    assert torch.isfinite(x).all()
+    op = W.Op("big", pool, 0, x, y0)
+    y, v = run_tc(dev, op, batch, mode, r)
+    if mode == "two_phase":
+        assert v.abs().max().item() > 65504.0, "the case does not reach past the fp16 range"
+    assert torch.isfinite(y).all()
+    check_op(op, batch, "sgmv", y, v if mode == "two_phase" else None, what=f"fp16 large v {mode}")
 
 
 def test_prefill_bad_offsets_launch_tc_but_write_nothing(dev):
