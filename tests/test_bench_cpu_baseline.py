@@ -38,3 +38,30 @@ def test_all_cores_sampler_covers_every_layer():
     assert per_step > 0
     assert layers == 3  # batches of 2 layers, then 1: the budget is not reached
     assert used == 2
+
+
+def _bench(args, **env):
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    e = dict(os.environ, **env)
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], capture_output=True, text=True,
+                       env=e, cwd=root, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    return [json.loads(ln) for ln in lines]
+
+
+def test_reference_arm_prints_one_line_on_rank0():
+    (line,) = _bench(["--impl", "reference", "--steps", "1", "--warmup", "1"])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "rows/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    assert _bench(["--impl", "reference", "--steps", "1", "--warmup", "1"], RANK="1", LOCAL_RANK="1",
+                  WORLD_SIZE="2") == []
