@@ -47,6 +47,7 @@ UNIT = "rows/s"
 WORKLOAD = ("Llama-2-7B decode step, bs32, r16, bf16, Distinct (32 adapters): SGMV delta of q,k,v,o,gate,up,down "
             "x 32 layers (224 ops)")
 FALLBACK_HBM = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ---------------------------------------------------------------------------------------------
@@ -59,6 +60,19 @@ def peaks():
         d = json.load(open(p))
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM, "fallback"
+
+
+def tensor_fraction(flops: float, secs: float) -> dict:
+    """Tensor-pipe roofline of a contraction timed in isolation: algorithmic flops / time against
+    the measured dense bf16 peak (cuBLAS, burst; fp16 has the same nominal rate)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        peak, src = float(json.load(open(p))["bf16_tflops"]), "measured bf16_tflops (cuBLAS, burst)"
+    else:
+        peak, src = FALLBACK_BF16_TFLOPS, "fallback"
+    achieved = flops / secs / 1e12
+    return {"achieved_tflops": round(achieved, 1), "peak_tflops": peak, "frac": round(achieved / peak, 4),
+            "peak_source": src}
 
 
 def dist_env():
@@ -340,6 +354,11 @@ def config_fractions(dev, stream, peak, iters=30):
         return C.op_bytes(d_in=op.pool.d_in, d_out=op.pool.d_out, row_ranks=[int(r[s]) for s in slots if s >= 0],
                           distinct_ranks=[int(r[s]) for s in np.unique(slots[slots >= 0])], v_roundtrip=v_roundtrip)
 
+    def op_flops_of(op, batch):
+        slots = batch.row_slot.cpu().numpy()
+        r = op.pool.rank.cpu().numpy()
+        return C.op_flops(d_in=op.pool.d_in, d_out=op.pool.d_out, row_ranks=[int(r[s]) for s in slots if s >= 0])
+
     def single(name, w, form):
         op = w.ops[0]
         h = m.make_pool(op.pool)
@@ -373,7 +392,7 @@ def config_fractions(dev, stream, peak, iters=30):
         del w, plan, g
         torch.cuda.empty_cache()
     w = W.sgmv_prefill_13b(device=dev)
-    tot_t, tot_b = 0.0, 0
+    tot_t, tot_b, tot_f = 0.0, 0, 0
     for op in w.ops:
         h = m.make_pool(op.pool)
         v = torch.empty((w.batch.M, op.pool.r_max), dtype=torch.float32, device=dev)
@@ -381,8 +400,10 @@ def config_fractions(dev, stream, peak, iters=30):
                                                      stream=s)
         tot_t += time_calls(fn, stream, 5, flush)
         tot_b += op_bytes_of(op, w.batch)
+        tot_f += op_flops_of(op, w.batch)
     res["4_prefill_13b"] = {"us_7_ops": round(tot_t * 1e6, 1), "bytes": tot_b, "gbs": round(tot_b / tot_t / 1e9, 1),
-                            "frac": round(tot_b / tot_t / 1e9 / peak, 4), "rows": w.batch.M}
+                            "frac": round(tot_b / tot_t / 1e9 / peak, 4), "rows": w.batch.M,
+                            "flops": tot_f, "tensor": tensor_fraction(tot_f, tot_t)}
     del w
     torch.cuda.empty_cache()
     single("5_paged_hetero_70b", W.paged_decode_70b(device=dev), "bgmv")

@@ -65,3 +65,16 @@ def test_reference_arm_prints_one_line_on_rank0():
 def test_reference_arm_other_ranks_print_nothing():
     assert _bench(["--impl", "reference", "--steps", "1", "--warmup", "1"], RANK="1", LOCAL_RANK="1",
                   WORLD_SIZE="2") == []
+
+
+def test_tensor_fraction_of_the_13b_prefill():
+    # 12604 rows at rank 64 over the 7 Llama-2-13B projections: 2 * rows * r * (d_in + d_out) each
+    import workloads.costmodel as C
+    w = W.sgmv_prefill_13b(device="cpu", projections=W.LLAMA2_13B[:1])
+    rows = w.batch.M
+    q = W.LLAMA2_13B[0]
+    flops = C.op_flops(d_in=q.d_in, d_out=q.d_out, row_ranks=[64] * rows)
+    assert flops == 2 * rows * 64 * (5120 + 5120)
+    t = bench.tensor_fraction(flops, 1e-3)
+    assert abs(t["achieved_tflops"] - flops / 1e-3 / 1e12) < 0.1
+    assert 0 < t["frac"] == round(t["achieved_tflops"] / t["peak_tflops"], 4)
