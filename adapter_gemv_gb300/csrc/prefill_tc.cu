@@ -1,19 +1,25 @@
 // prefill_tc.cu -- tensor-core path for long SGMV segments (prefill), sm_103a.
 //
-// A segment of L >= 128 rows that shares one adapter is a real dense contraction ("the segments
-// are short and fat, so the work is closer to a GEMM", "Multi-LoRA Serving, in depth", section
-// "Two shapes: SGMV for prefill, BGMV for decode"; Punica section 3.4, "Tensor Core usage"). Its
-// full 128-row blocks run here; the ragged tail of each segment runs on the CUDA-core kernels.
+// A long segment that shares one adapter is a real dense contraction ("the segments are short
+// and fat, so the work is closer to a GEMM", "Multi-LoRA Serving, in depth", section "Two shapes:
+// SGMV for prefill, BGMV for decode"; Punica section 3.4, "Tensor Core usage"). Segments of at
+// least kTcMinRows rows run here in 128-row tiles, the last one masked; shorter segments run on
+// the CUDA-core kernels. bf16 and fp16 stacked pools; the MMAs are kind::f16 with both operands of
+// the pool's type and fp32 accumulators.
 //
 //   shrink  V[128 x r] = X[128 x d_in] . A   : one CTA per (tile, K part); a cluster of K parts
 //           sums its fp32 partials through distributed shared memory. X tiles and A^T rows are
-//           both K-major; TMA (128-byte swizzle) feeds a 4-stage mbarrier ring, one thread issues
-//           tcgen05.mma (M = 128, N = rank rounded up to 16, K = 16 per instruction) into a TMEM
-//           accumulator, and all four warps read it back with tcgen05.ld.
-//   expand  Y[128 x 128] += scale . V[128 x r] . B[r x 128] : one CTA per (tile, run of N blocks).
-//           V (fp32) is split into bf16 hi + lo parts, so the product keeps ~16 bits of v, and
-//           both parts are multiplied into one fp32 accumulator. B rows are an MN-major operand
-//           loaded by TMA; y is read and written by the epilogue threads (one row each).
+//           both K-major; TMA (128-byte swizzle) feeds an mbarrier ring as deep as shared memory
+//           allows, two swizzle atoms (128 K elements) per stage; one thread issues tcgen05.mma
+//           (M = 128, N = rank rounded up to 16, K = 16 per instruction) into a TMEM accumulator,
+//           and all four warps read it back with tcgen05.ld.
+//   expand  Y[128 x 64] += scale . V[128 x r] . B[r x 64] per block : one CTA per (tile, run of
+//           64-column blocks), in warp roles: a producer lane TMA-loads each block's y tile and B
+//           rows into a ring of buffers, an MMA lane multiplies into one of two TMEM accumulators,
+//           eight epilogue warps add the result into the y tile in shared memory (rounded once),
+//           and a store lane TMA-stores it and frees the buffer. V (fp32) is split into hi + lo
+//           parts of the pool's type, both multiplied into the fp32 accumulator; fp16 rows of V are
+//           first scaled by a power of two so that they cannot overflow.
 // Every wait is bounded; a timed-out CTA reports MLORA_STATUS_TIMEOUT and writes nothing.
 #include <cuda.h>
 #include <cuda_runtime.h>
