@@ -409,6 +409,31 @@ def pin_sampled_rows(orc, seed=26):
     assert np.array_equal(part[0][others], y[others]) and np.all(np.isnan(part[1][others]))
 
 
+def pin_sgmv_equals_bgmv_on_the_same_rows(orc, seed=27):
+    """The two forms state one computation (Punica section 3.4: a segment is a run of rows with one
+    adapter; "Multi-LoRA Serving, in depth": a slot per row): SGMV over random segments (empty,
+    repeated slots, -1) and BGMV with each row's slot taken from its segment give the same bits,
+    on stacked and paged pools, in both dtypes."""
+    rng = np.random.default_rng(seed)
+    for dt in (BF16, FP16):
+        for paged in (False, True):
+            S, L, R, d_in, d_out, M = 5, 2, 8, 40, 24, 23
+            pool, _, _ = random_pool(rng, dt, S, L, R, d_in, d_out, ranks=rng.integers(1, R + 1, S))
+            if paged:
+                pool = to_paged(pool, rng)
+            cuts = np.sort(rng.integers(0, M + 1, 6))
+            off = np.r_[0, cuts, M].astype(np.int32)
+            ss = rng.integers(-1, S, len(off) - 1).astype(np.int32)
+            row_slot = np.repeat(ss, np.diff(off)).astype(np.int32)
+            x, y = random_act(rng, dt, M, d_in), random_act(rng, dt, M, d_out)
+            for layer in range(L):
+                ys, vs, _, sts = orc.sgmv(pool, layer, x, y, off, ss)
+                yb, vb, _, stb = orc.bgmv(pool, layer, x, y, row_slot)
+                assert sts == 0 and stb == 0
+                assert np.array_equal(ys, yb), f"y differs between the forms (dtype {dt}, paged {paged})"
+                assert np.array_equal(vs, vb, equal_nan=True), "v differs between the forms"
+
+
 ALL_PINS = [pin_decode_exhaustive, pin_round_trip_exhaustive, pin_round_matches_library, pin_round_ties,
             pin_identical_is_dense_gemm, pin_merged_identity, pin_rank_closed_form, pin_slot_identification,
-            pin_skip_rows_untouched, pin_status_contract, pin_sampled_rows]
+            pin_skip_rows_untouched, pin_status_contract, pin_sampled_rows, pin_sgmv_equals_bgmv_on_the_same_rows]

@@ -41,7 +41,8 @@ MUTANTS = {
 
 # the operator pins run first: they are cheap and catch most mutants
 ORDER = [P.pin_rank_closed_form, P.pin_slot_identification, P.pin_identical_is_dense_gemm, P.pin_merged_identity,
-         P.pin_skip_rows_untouched, P.pin_status_contract, P.pin_sampled_rows, P.pin_round_ties,
+         P.pin_skip_rows_untouched, P.pin_status_contract, P.pin_sampled_rows, P.pin_sgmv_equals_bgmv_on_the_same_rows,
+         P.pin_round_ties,
          P.pin_round_trip_exhaustive, P.pin_decode_exhaustive, P.pin_round_matches_library]
 
 
