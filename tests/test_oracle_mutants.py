@@ -37,6 +37,12 @@ MUTANTS = {
     "truncating_round": ("if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;", ""),
     "subnormal_decode_off_by_one": ("ldexp((double)m, 1 - f.bias - f.mant_bits)", "ldexp((double)m, -f.bias - f.mant_bits)"),
     "overflow_threshold_low": ("if (r >= ldexp(1.0, emax + 1))", "if (r > ldexp(1.0, emax))"),
+    "bgmv_slot_of_next_row": ("int32_t s = off ? sgmv_row_slot(off, seg_slot, nseg, i) : row_slot[i];",
+                              "int32_t s = off ? sgmv_row_slot(off, seg_slot, nseg, i) : row_slot[i + 1 < M ? i + 1 : i];"),
+    "shrink_drops_top_rank_row": ("int r = p->rank[s];\n  for (int j = 0; j < r; ++j) {\n    double acc = 0.0;",
+                                  "int r = p->rank[s] - 1;\n  for (int j = 0; j < r; ++j) {\n    double acc = 0.0;"),
+    "x_element_shifted": ("acc += orc_decode(x_row[k], p->dtype) * elem_a(p, s, layer, k, j);",
+                          "acc += orc_decode(x_row[k > 0 ? k - 1 : 0], p->dtype) * elem_a(p, s, layer, k, j);"),
 }
 
 # the operator pins run first: they are cheap and catch most mutants
