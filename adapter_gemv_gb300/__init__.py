@@ -28,6 +28,7 @@ MLORA_MAX_RANK = 128
 STATUS_BAD_OFFSETS, STATUS_BAD_SLOT, STATUS_BAD_RANK, STATUS_BAD_PAGE, STATUS_TIMEOUT = 1, 2, 4, 8, 16
 ERR_NULL, ERR_DTYPE, ERR_SHAPE, ERR_ALIGN, ERR_POOL, ERR_CUDA, ERR_TOO_LARGE = -1, -2, -3, -4, -5, -6, -7
 NOALLOC_MAX_FLOATS = 1 << 20
+LAUNCH_PROGRAMMATIC = 1
 
 _DT = {torch.bfloat16: MLORA_BF16, torch.float16: MLORA_FP16}
 
@@ -52,6 +53,12 @@ class mlora_problem(ctypes.Structure):
                 ("pool", ctypes.POINTER(mlora_pool)), ("layer", ctypes.c_int32), ("v_scratch", ctypes.c_void_p)]
 
 
+class mlora_group(ctypes.Structure):
+    _fields_ = [("problems", ctypes.POINTER(mlora_problem)), ("num_problems", ctypes.c_int32),
+                ("seg_offsets", ctypes.c_void_p), ("seg_slot", ctypes.c_void_p), ("num_segments", ctypes.c_int32),
+                ("num_rows", ctypes.c_int32)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -66,8 +73,8 @@ SIGNATURES = {
     "lora_bgmv": [_V, _I64, _V, _I64, _PP, _V, _I32, _I32, _V, _V, _V],
     "lora_sgmv_noalloc": [_V, _I64, _V, _I64, _PP, _V, _V, _I32, _I32, _I32, _V, _V],
     "lora_sgmv_grouped": [ctypes.POINTER(mlora_problem), _I32, _V, _V, _I32, _I32, _V, _V],
-    "lora_sgmv_grouped_prefetch": [ctypes.POINTER(mlora_problem), _I32, ctypes.POINTER(mlora_problem), _I32, _V, _V,
-                                   _I32, _I32, _V, _V],
+    "lora_sgmv_grouped_ex": [ctypes.POINTER(mlora_problem), _I32, _V, _V, _I32, _I32, ctypes.c_uint32, _V, _V],
+    "lora_sgmv_sequence": [ctypes.POINTER(mlora_group), _I32, ctypes.c_uint32, _V, _V],
 }
 
 
@@ -90,6 +97,8 @@ def lib():
                 L.lora_launch_count.restype = ctypes.c_int64
                 L.lora_set_programmatic_launch.argtypes = [ctypes.c_int]
                 L.lora_set_programmatic_launch.restype = ctypes.c_int
+                L.lora_test_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+                L.lora_test_set_wait_limit_ns.restype = None
                 _lib = L
     return _lib
 
@@ -220,11 +229,12 @@ def lora_bgmv(y, x, pool, row_slot, layer, v_scratch, status=None, stream=None):
 
 
 class Group:
-    """A prepared lora_sgmv_grouped call: the problem array is built once and reused.
-    set_next() attaches the L2 prefetch hint (lora_sgmv_grouped_prefetch)."""
+    """A prepared lora_sgmv_grouped_ex call: the problem array is built once and reused."""
 
-    def __init__(self, problems: Sequence[tuple], seg_offsets, seg_slot, num_rows: int, status=None):
-        """problems: (y, x, pool, layer, v_scratch) tuples sharing the rows' segments."""
+    def __init__(self, problems: Sequence[tuple], seg_offsets, seg_slot, num_rows: int, status=None,
+                 programmatic: bool = False):
+        """problems: (y, x, pool, layer, v_scratch) tuples sharing the rows' segments.
+        programmatic: launch with programmatic dependent launch (LAUNCH_PROGRAMMATIC)."""
         if not 1 <= len(problems) <= MLORA_MAX_GROUP:
             raise ValueError(f"a group holds 1..{MLORA_MAX_GROUP} problems")
         self.handles = [make_pool(p[2]) for p in problems]
@@ -241,16 +251,12 @@ class Group:
         self.off, self.slot = _i32(seg_offsets, "seg_offsets"), _i32(seg_slot, "seg_slot")
         self.nseg, self.M = int(seg_slot.numel()), int(num_rows)
         self.status = _i32(status, "status")
-        self.fn = lib().lora_sgmv_grouped_prefetch
-        self.next_arr, self.nnext = None, 0
-
-    def set_next(self, other: "Group"):
-        """Prefetch hint: `other` is the call that follows this one on the same stream."""
-        self.next_arr, self.nnext = (other.arr, other.n) if other is not None else (None, 0)
+        self.flags = LAUNCH_PROGRAMMATIC if programmatic else 0
+        self.fn = lib().lora_sgmv_grouped_ex
 
     def __call__(self, stream=None):
-        _check(self.fn(self.arr, self.n, self.next_arr, self.nnext, self.off, self.slot, self.nseg, self.M,
-                       self.status, _stream(stream)))
+        _check(self.fn(self.arr, self.n, self.off, self.slot, self.nseg, self.M, self.flags, self.status,
+                       _stream(stream)))
 
 
 def lora_sgmv_grouped(problems, seg_offsets, seg_slot, status=None, stream=None):
@@ -259,13 +265,36 @@ def lora_sgmv_grouped(problems, seg_offsets, seg_slot, status=None, stream=None)
     _check(lib().lora_sgmv_grouped(g.arr, g.n, g.off, g.slot, g.nseg, g.M, g.status, _stream(stream)))
 
 
-def lora_sgmv_grouped_prefetch(problems, next_problems, seg_offsets, seg_slot, status=None, stream=None):
-    """Grouped call plus the L2 prefetch hint for the call that follows (same rows)."""
+def lora_sgmv_grouped_ex(problems, seg_offsets, seg_slot, flags: int = 0, status=None, stream=None):
     num_rows = int(problems[0][0].shape[0])
     g = Group(problems, seg_offsets, seg_slot, num_rows, status)
-    if next_problems:
-        g.set_next(Group(next_problems, seg_offsets, seg_slot, num_rows))
-    g(stream)
+    _check(lib().lora_sgmv_grouped_ex(g.arr, g.n, g.off, g.slot, g.nseg, g.M, int(flags), g.status,
+                                      _stream(stream)))
+
+
+class CallSequence:
+    """A prepared lora_sgmv_sequence call: the grouped calls of a whole step, issued by one call
+    into the library (which launches them in order from native code)."""
+
+    def __init__(self, groups: "Sequence[Group]", programmatic: bool = False, status=None):
+        self.groups = list(groups)
+        self.arr = (mlora_group * len(self.groups))()
+        for a, g in zip(self.arr, self.groups):
+            a.problems = ctypes.cast(g.arr, ctypes.POINTER(mlora_problem))
+            a.num_problems = g.n
+            a.seg_offsets, a.seg_slot = g.off, g.slot
+            a.num_segments, a.num_rows = g.nseg, g.M
+        self.flags = LAUNCH_PROGRAMMATIC if programmatic else 0
+        self.status = _i32(status, "status")
+        self.fn = lib().lora_sgmv_sequence
+
+    def __call__(self, stream=None):
+        _check(self.fn(self.arr, len(self.groups), self.flags, self.status, _stream(stream)))
+
+
+def lora_sgmv_sequence(groups, programmatic: bool = False, status=None, stream=None):
+    """groups: prepared Group objects (each a grouped call over its rows), issued in order."""
+    CallSequence(groups, programmatic, status)(stream)
 
 
 def launch_count() -> int:
@@ -273,9 +302,15 @@ def launch_count() -> int:
 
 
 def lora_set_programmatic_launch(enable: bool) -> bool:
-    """Process-wide switch for programmatic dependent launch (see include/mlora.h); returns the
-    previous setting."""
+    """Programmatic dependent launch for the calling thread's later calls (see include/mlora.h);
+    returns this thread's previous setting."""
     return bool(lib().lora_set_programmatic_launch(1 if enable else 0))
+
+
+def lora_test_set_wait_limit_ns(limit_ns: int) -> None:
+    """Testing hook: time limit of the CUDA-core kernels' waits for this thread's later calls
+    (0 = the default). Only the tests of the time-out path use it."""
+    lib().lora_test_set_wait_limit_ns(int(limit_ns))
 
 
 def abi_version() -> int:

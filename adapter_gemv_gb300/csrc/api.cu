@@ -7,9 +7,10 @@
 
 #include <atomic>
 #include <cstdint>
-#include <mutex>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "launch.h"
 #include "mlora.h"
@@ -18,7 +19,8 @@ namespace {
 
 thread_local char g_cuda_err[256] = "no CUDA error recorded";
 std::atomic<int64_t> g_launches{0};
-std::atomic<int> g_pdl{0};
+thread_local int g_pdl = 0;              // programmatic dependent launch for this thread's calls
+thread_local uint64_t g_wait_limit_ns = 0;  // testing hook: 0 = the kernels' default limit
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -130,56 +132,63 @@ mlora::DecodeParams base_params(const int32_t *off, const int32_t *seg_slot, int
   return d;
 }
 
-int run(int mode, int dtype, const mlora::DecodeParams &d, void *stream) {
-  const cudaError_t e = mlora::launch_decode(mode, dtype, d, static_cast<cudaStream_t>(stream), g_pdl.load() != 0);
+int run(int mode, int dtype, mlora::DecodeParams d, void *stream, bool pdl) {
+  d.wait_ns = g_wait_limit_ns;
+  const cudaError_t e = mlora::launch_decode(mode, dtype, d, static_cast<cudaStream_t>(stream), pdl);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return MLORA_OK;
 }
 
-mlora::ProblemDev problem(const mlora_pool *pool, int32_t layer, const void *x, int64_t ldx, void *y, int64_t ldy,
-                          float *v);
-
-// SGMV with long segments: segments of at least kTcMinRows rows on the tensor cores (128-row
-// blocks, the last one masked), shorter ones on the CUDA-core kernel. mode selects the phases.
-int run_sgmv(int mode, const mlora_pool *pool, int32_t layer, const void *x, int64_t ldx, void *y, int64_t ldy,
-             float *v, const int32_t *off, const int32_t *seg_slot, int32_t nseg, int32_t num_rows, int32_t *status,
-             void *stream) {
-  mlora::DecodeParams d = base_params(off, seg_slot, nseg, nullptr, num_rows, status);
-  d.prob[0] = problem(pool, layer, x, ldx, y, ldy, v);
-  d.nprob = 1;
-  if (mlora::tc_eligible(d.prob[0].pool, num_rows, nseg)) {
-    mlora::TcParams tp{};
-    tp.num_slots = pool->num_slots;
-    tp.num_layers = pool->num_layers;
-    tp.r_max = pool->r_max;
-    tp.d_in = pool->d_in;
-    tp.d_out = pool->d_out;
-    tp.layer = layer;
-    tp.rank = pool->rank;
-    tp.scale = pool->scale;
-    tp.seg_off = off;
-    tp.seg_slot = seg_slot;
-    tp.nseg = nseg;
-    tp.M = num_rows;
-    tp.v = v;
-    tp.y = static_cast<uint16_t *>(y);
-    tp.ldy = ldy;
-    tp.status = status;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (mode != mlora::MODE_EXPAND) {
-      const cudaError_t e = mlora::launch_tc_shrink(d.prob[0], tp, st);
-      if (e != cudaSuccess) return cuda_fail(e, "tensor-core shrink launch");
-      g_launches.fetch_add(1, std::memory_order_relaxed);
-    }
-    if (mode != mlora::MODE_SHRINK) {
-      const cudaError_t e = mlora::launch_tc_expand(d.prob[0], tp, st);
-      if (e != cudaSuccess) return cuda_fail(e, "tensor-core expand launch");
-      g_launches.fetch_add(1, std::memory_order_relaxed);
-    }
-    d.tc_min = mlora::kTcMinRows;
+// The tensor-core kernels for the long segments of one problem (prefill_tc.cu): segments of at
+// least kTcMinRows rows, in 128-row blocks (the last one masked). Marks the problem so that the
+// CUDA-core kernel launched after them takes only the shorter segments.
+int run_tc(int mode, mlora::ProblemDev &q, const mlora_pool *pool, const int32_t *off, const int32_t *seg_slot,
+           int32_t nseg, int32_t num_rows, int32_t *status, void *stream) {
+  mlora::TcParams tp{};
+  tp.num_slots = pool->num_slots;
+  tp.num_layers = pool->num_layers;
+  tp.r_max = pool->r_max;
+  tp.d_in = pool->d_in;
+  tp.d_out = pool->d_out;
+  tp.layer = q.layer;
+  tp.rank = pool->rank;
+  tp.scale = pool->scale;
+  tp.seg_off = off;
+  tp.seg_slot = seg_slot;
+  tp.nseg = nseg;
+  tp.M = num_rows;
+  tp.v = q.v;
+  tp.y = q.y;
+  tp.ldy = q.ldy;
+  tp.status = status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (mode != mlora::MODE_EXPAND) {
+    const cudaError_t e = mlora::launch_tc_shrink(q, tp, st);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core shrink launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
   }
-  return run(mode, pool->dtype, d, stream);
+  if (mode != mlora::MODE_SHRINK) {
+    const cudaError_t e = mlora::launch_tc_expand(q, tp, st);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core expand launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  q.tc_min = mlora::kTcMinRows;
+  return MLORA_OK;
+}
+
+// SGMV over the problems of d: for each problem whose batch may hold long segments (a prefill
+// batch, or prefill and decode rows mixed), the tensor-core kernels take the segments of at least
+// kTcMinRows rows; then one CUDA-core launch takes every other segment of every problem.
+int run_sgmv(int mode, mlora::DecodeParams &d, const mlora_pool *const *pools, void *stream, bool pdl) {
+  bool any_tc = false;
+  for (int q = 0; q < d.nprob; ++q) {
+    if (!mlora::tc_eligible(d.prob[q].pool, d.M, d.nseg)) continue;
+    TRY(run_tc(mode, d.prob[q], pools[q], d.seg_off, d.seg_slot, d.nseg, d.M, d.status, stream));
+    any_tc = true;
+  }
+  // after a tensor-core launch the decode kernel's dependency is that launch (no PDL needed)
+  return run(mode, pools[0]->dtype, d, stream, pdl && !any_tc);
 }
 
 mlora::ProblemDev problem(const mlora_pool *pool, int32_t layer, const void *x, int64_t ldx, void *y, int64_t ldy,
@@ -230,8 +239,10 @@ int lora_sgmv_shrink(float *v, const void *x, int64_t ldx, const mlora_pool *poo
   TRY(check_x(x, ldx, pool, num_rows));
   TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
-  return run_sgmv(mlora::MODE_SHRINK, pool, layer, x, ldx, nullptr, 0, v, seg_offsets, seg_slot, num_segments,
-                  num_rows, dev_status, stream);
+  mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
+  d.prob[0] = problem(pool, layer, x, ldx, nullptr, 0, v);
+  d.nprob = 1;
+  return run_sgmv(mlora::MODE_SHRINK, d, &pool, stream, g_pdl != 0);
 }
 
 int lora_sgmv_expand(void *y, int64_t ldy, const float *v, const mlora_pool *pool, const int32_t *seg_offsets,
@@ -242,8 +253,10 @@ int lora_sgmv_expand(void *y, int64_t ldy, const float *v, const mlora_pool *poo
   TRY(check_y(y, ldy, pool, num_rows));
   TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
-  return run_sgmv(mlora::MODE_EXPAND, pool, layer, nullptr, 0, y, ldy, const_cast<float *>(v), seg_offsets, seg_slot,
-                  num_segments, num_rows, dev_status, stream);
+  mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
+  d.prob[0] = problem(pool, layer, nullptr, 0, y, ldy, const_cast<float *>(v));
+  d.nprob = 1;
+  return run_sgmv(mlora::MODE_EXPAND, d, &pool, stream, g_pdl != 0);
 }
 
 int lora_bgmv_shrink(float *v, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
@@ -256,7 +269,7 @@ int lora_bgmv_shrink(float *v, const void *x, int64_t ldx, const mlora_pool *poo
   mlora::DecodeParams d = base_params(nullptr, nullptr, 0, row_slot, num_rows, dev_status);
   d.prob[0] = problem(pool, layer, x, ldx, nullptr, 0, v);
   d.nprob = 1;
-  return run(mlora::MODE_SHRINK, pool->dtype, d, stream);
+  return run(mlora::MODE_SHRINK, pool->dtype, d, stream, g_pdl != 0);
 }
 
 int lora_bgmv_expand(void *y, int64_t ldy, const float *v, const mlora_pool *pool, const int32_t *row_slot,
@@ -269,7 +282,7 @@ int lora_bgmv_expand(void *y, int64_t ldy, const float *v, const mlora_pool *poo
   mlora::DecodeParams d = base_params(nullptr, nullptr, 0, row_slot, num_rows, dev_status);
   d.prob[0] = problem(pool, layer, nullptr, 0, y, ldy, const_cast<float *>(v));
   d.nprob = 1;
-  return run(mlora::MODE_EXPAND, pool->dtype, d, stream);
+  return run(mlora::MODE_EXPAND, pool->dtype, d, stream, g_pdl != 0);
 }
 
 int lora_sgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *seg_offsets,
@@ -281,8 +294,10 @@ int lora_sgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool
   TRY(check_y(y, ldy, pool, num_rows));
   TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
-  return run_sgmv(mlora::MODE_FUSED, pool, layer, x, ldx, y, ldy, v_scratch, seg_offsets, seg_slot, num_segments,
-                  num_rows, dev_status, stream);
+  mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
+  d.prob[0] = problem(pool, layer, x, ldx, y, ldy, v_scratch);
+  d.nprob = 1;
+  return run_sgmv(mlora::MODE_FUSED, d, &pool, stream, g_pdl != 0);
 }
 
 int lora_sgmv_noalloc(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool,
@@ -296,8 +311,10 @@ int lora_sgmv_noalloc(void *y, int64_t ldy, const void *x, int64_t ldx, const ml
   if (num_rows == 0) return MLORA_OK;
   float *v = nullptr;
   TRY(noalloc_scratch(&v));
-  return run_sgmv(mlora::MODE_FUSED, pool, layer, x, ldx, y, ldy, v, seg_offsets, seg_slot, num_segments, num_rows,
-                  dev_status, stream);
+  mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
+  d.prob[0] = problem(pool, layer, x, ldx, y, ldy, v);
+  d.nprob = 1;
+  return run_sgmv(mlora::MODE_FUSED, d, &pool, stream, g_pdl != 0);
 }
 
 int lora_bgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
@@ -311,18 +328,21 @@ int lora_bgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool
   mlora::DecodeParams d = base_params(nullptr, nullptr, 0, row_slot, num_rows, dev_status);
   d.prob[0] = problem(pool, layer, x, ldx, y, ldy, v_scratch);
   d.nprob = 1;
-  return run(mlora::MODE_FUSED, pool->dtype, d, stream);
+  return run(mlora::MODE_FUSED, pool->dtype, d, stream, g_pdl != 0);
 }
 
-int lora_sgmv_grouped_prefetch(const mlora_problem *problems, int32_t num_problems, const mlora_problem *next,
-                               int32_t num_next, const int32_t *seg_offsets, const int32_t *seg_slot,
-                               int32_t num_segments, int32_t num_rows, int32_t *dev_status, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Validates one grouped call and fills its parameter block (no launch).
+int prepare_grouped(const mlora_problem *problems, int32_t num_problems, const int32_t *seg_offsets,
+                    const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t *dev_status,
+                    mlora::DecodeParams &d, const mlora_pool **pools) {
   if (!problems) return MLORA_ERR_NULL;
   if (num_problems < 1 || num_problems > MLORA_MAX_GROUP) return MLORA_ERR_SHAPE;
-  if (num_next < 0 || num_next > MLORA_MAX_GROUP) return MLORA_ERR_SHAPE;
-  if (num_next > 0 && !next) return MLORA_ERR_NULL;
   TRY(check_rows_sgmv(seg_offsets, seg_slot, num_segments, num_rows, dev_status));
-  mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
+  d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
   for (int q = 0; q < num_problems; ++q) {
     const mlora_problem &pb = problems[q];
     TRY(check_pool(pb.pool, pb.layer, true, true));
@@ -331,23 +351,57 @@ int lora_sgmv_grouped_prefetch(const mlora_problem *problems, int32_t num_proble
     TRY(check_x(pb.x, pb.ldx, pb.pool, num_rows));
     TRY(check_y(pb.y, pb.ldy, pb.pool, num_rows));
     d.prob[q] = problem(pb.pool, pb.layer, pb.x, pb.ldx, pb.y, pb.ldy, pb.v_scratch);
+    pools[q] = pb.pool;
   }
   d.nprob = num_problems;
-  for (int q = 0; q < num_next; ++q) {
-    TRY(check_pool(next[q].pool, next[q].layer, true, true));
-    d.next_pool[q] = to_dev(next[q].pool);
-    d.next_layer[q] = next[q].layer;
-  }
-  d.nnext = num_next;
+  return MLORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lora_sgmv_grouped_ex(const mlora_problem *problems, int32_t num_problems, const int32_t *seg_offsets,
+                         const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, uint32_t flags,
+                         int32_t *dev_status, void *stream) {
+  if (flags & ~MLORA_LAUNCH_PROGRAMMATIC) return MLORA_ERR_SHAPE;
+  mlora::DecodeParams d;
+  const mlora_pool *pools[MLORA_MAX_GROUP];
+  TRY(prepare_grouped(problems, num_problems, seg_offsets, seg_slot, num_segments, num_rows, dev_status, d, pools));
   if (num_rows == 0) return MLORA_OK;
-  return run(mlora::MODE_FUSED, problems[0].pool->dtype, d, stream);
+  return run_sgmv(mlora::MODE_FUSED, d, pools, stream, (flags & MLORA_LAUNCH_PROGRAMMATIC) != 0);
+}
+
+int lora_sgmv_sequence(const mlora_group *groups, int32_t num_groups, uint32_t flags, int32_t *dev_status,
+                       void *stream) {
+  if (!groups) return MLORA_ERR_NULL;
+  if (num_groups < 0) return MLORA_ERR_SHAPE;
+  if (flags & ~MLORA_LAUNCH_PROGRAMMATIC) return MLORA_ERR_SHAPE;
+  struct Prepared {
+    mlora::DecodeParams d;
+    const mlora_pool *pools[MLORA_MAX_GROUP];
+  };
+  std::vector<Prepared> calls((size_t)num_groups);
+  for (int g = 0; g < num_groups; ++g) {
+    const mlora_group &gr = groups[g];
+    TRY(prepare_grouped(gr.problems, gr.num_problems, gr.seg_offsets, gr.seg_slot, gr.num_segments, gr.num_rows,
+                        dev_status, calls[g].d, calls[g].pools));
+  }
+  bool first = true;
+  for (int g = 0; g < num_groups; ++g) {
+    if (groups[g].num_rows == 0) continue;
+    const bool pdl = (flags & MLORA_LAUNCH_PROGRAMMATIC) != 0 && !first;
+    TRY(run_sgmv(mlora::MODE_FUSED, calls[g].d, calls[g].pools, stream, pdl));
+    first = false;
+  }
+  return MLORA_OK;
 }
 
 int lora_sgmv_grouped(const mlora_problem *problems, int32_t num_problems, const int32_t *seg_offsets,
                       const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t *dev_status,
                       void *stream) {
-  return lora_sgmv_grouped_prefetch(problems, num_problems, nullptr, 0, seg_offsets, seg_slot, num_segments, num_rows,
-                                    dev_status, stream);
+  return lora_sgmv_grouped_ex(problems, num_problems, seg_offsets, seg_slot, num_segments, num_rows,
+                              g_pdl ? MLORA_LAUNCH_PROGRAMMATIC : 0u, dev_status, stream);
 }
 
 const char *lora_error_string(int code) {
@@ -366,7 +420,13 @@ const char *lora_error_string(int code) {
 
 int lora_abi_version(void) { return MLORA_ABI_VERSION; }
 
-int lora_set_programmatic_launch(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
+int lora_set_programmatic_launch(int enable) {
+  const int prev = g_pdl;
+  g_pdl = enable ? 1 : 0;
+  return prev;
+}
+
+void lora_test_set_wait_limit_ns(uint64_t limit_ns) { g_wait_limit_ns = limit_ns; }
 
 int64_t lora_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

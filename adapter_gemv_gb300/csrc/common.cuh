@@ -131,9 +131,52 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Default limit of a wait on data this kernel (or its cluster) is about to receive, and the limit
+// of the waits that drain copies still in flight before a CTA that gave up exits.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+
+// Non-blocking probes of a phase (mbarrier.test_wait): true once the phase with the given parity
+// has completed. Unlike try_wait they never suspend the thread.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this are served by polling with test_wait and reading the clock at every poll:
+// try_wait may suspend the thread for longer than such a limit.
+constexpr uint64_t kShortLimitNs = 1000ull;
+
 // Wait for the phase with the given parity to complete, for at most `limit_ns` nanoseconds.
 // Returns false on timeout (the caller reports MLORA_STATUS_TIMEOUT and stops using the stage).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+// The clock is read every 256 polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+  if (limit_ns < kShortLimitNs) {
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+      if (mbar_test(bar, parity)) return true;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -155,8 +198,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
   return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity,
-                                                  uint64_t limit_ns = 2000000000ull) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+  if (limit_ns < kShortLimitNs) {
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+      if (mbar_test_cluster(bar, parity)) return true;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {

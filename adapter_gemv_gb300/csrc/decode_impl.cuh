@@ -35,6 +35,9 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -119,7 +122,7 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
     ti->nr = 0;
   }
   __syncthreads();
-  if (sgmv && p.rt == 1 && p.tc_min == 0 && p.nseg <= SCAN_CAP) {
+  if (sgmv && p.rt == 1 && pr.tc_min == 0 && p.nseg <= SCAN_CAP) {
     // One-row tiles, every segment here: tile t is row t, in the segment whose offset is the last
     // one <= t (one ballot per 32 offsets); the offsets are checked the same way.
     if (warp == 0) {
@@ -166,7 +169,7 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
             lo = scan[q];
             len = scan[q + 1] - lo;
             if (len < 0 || lo < 0 || scan[q + 1] > p.M) bad = 1;
-            if (p.tc_min > 0 && len >= p.tc_min) len = 0;  // a tensor-core kernel does this segment
+            if (pr.tc_min > 0 && len >= pr.tc_min) len = 0;  // a tensor-core kernel does this segment
           }
           const int32_t nt = (q < cnt && len > 0) ? (len + p.rt - 1) / p.rt : 0;
           int32_t incl = nt;
@@ -323,6 +326,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool clustered = (MODE != MODE_EXPAND) && cs > 1;
+  const uint64_t wlim = p.wait_ns ? p.wait_ns : kWaitLimitNs;  // limit of the waits below
   const uint32_t c = (MODE == MODE_EXPAND) ? (blockIdx.x % cs) : cluster_ctarank();
   const int64_t unit = blockIdx.x / cs;  // (problem, tile)
   const int prob = (int)(unit / p.tiles);
@@ -342,7 +346,6 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   pdl_launch_dependents();                  // the next kernel may start; it waits for us before reading our outputs
 
   resolve_tile<MODE>(p, pr, t, ti, scan, rank_c, scale_c);
-  if (c == 0 && tid == 0 && ti->bad) report(p.status, ti->bad);
   const bool active = !ti->skip;  // uniform across the block and across the cluster
   const int row0 = ti->row0, nr = ti->nr, s = ti->slot, rank = ti->rank;
   const float scale = ti->scale;
@@ -412,34 +415,6 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
         prefetch_l2(a_row(pl, s, pr.layer, j) + k_begin + kbn, (uint32_t)(k_end - k_begin - kbn) * 2);
     if (clustered && lane == 0) mbar_arrive_expect_tx(xbar, (uint32_t)(cs * nr * rank * 4));
   }
-  // Prefetch hint: the adapter rows the next call will read for this tile's slot, shared out
-  // over the nprob * cs CTAs of this tile (row items round-robin).
-  if (active && p.nnext > 0 && warp == 1) {
-    const int W = p.nprob * cs, w = prob * cs + (int)c;
-    for (int q = 0; q < p.nnext; ++q) {
-      const PoolDev &np = p.next_pool[q];
-      if (s >= np.num_slots) continue;
-      const int nrank = np.rank[s];
-      if (nrank < 1 || nrank > np.r_max) continue;
-      for (int item = lane; item < 2 * nrank; item += 32) {
-        if ((q * 2 * nrank + item) % W != w) continue;
-        const int j = item >> 1;
-        const int64_t tix = ((int64_t)s * np.num_layers + p.next_layer[q]) * np.r_max + j;
-        if (item & 1) {
-          const int64_t pg = np.kind == MLORA_POOL_STACKED ? 0 : np.b_tab[tix];
-          if (np.kind == MLORA_POOL_PAGED && (pg < 0 || pg >= np.num_pages)) continue;
-          prefetch_l2(np.kind == MLORA_POOL_STACKED ? np.b + tix * np.d_out : np.pages + pg * np.page_elems,
-                      (uint32_t)np.d_out * 2);
-        } else {
-          const int64_t pg = np.kind == MLORA_POOL_STACKED ? 0 : np.a_tab[tix];
-          if (np.kind == MLORA_POOL_PAGED && (pg < 0 || pg >= np.num_pages)) continue;
-          prefetch_l2(np.kind == MLORA_POOL_STACKED ? np.a_t + tix * np.d_in : np.pages + pg * np.page_elems,
-                      (uint32_t)np.d_in * 2);
-        }
-      }
-    }
-  }
-
   // A registers: in the Rows<JN> layout, register i = jj * (16 / JN) + u holds chunk
   // c8 = lane + 32 u of rank row j = warp + NWARPS jj (a[i / UK][i % UK]; JN = JPW is [jj][u]).
   uint4 a[JPW][UK];
@@ -482,6 +457,9 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   }
 
   pdl_wait();  // the previous kernel in the stream has finished; its writes are visible
+  // The status word is an output: written only after the wait (the previous kernel may be
+  // clearing it).
+  if (c == 0 && tid == 0 && ti->bad) report(p.status, ti->bad);
 
   if (tid == 0) {
     if (x_bulk) {
@@ -510,7 +488,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       // chunks in mixed-precision FMAs (16-bit operands, fp32 sums; no unpacking), two chains
       // per (row, rank row). No guards: A is zero outside the slice and the rank, x is zero in
       // rows past nr and past the slice, so every chunk and row runs unconditionally.
-      const int ok = mbar_wait(ibar, 0) ? 1 : 0;
+      const int ok = mbar_wait(ibar, 0, wlim) ? 1 : 0;
       timed_out = __syncthreads_or(!ok);
       if (!timed_out) {
         float c0[RT][JPW], c1[RT][JPW];
@@ -536,7 +514,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       // The x slice is in shared memory; A comes in passes of KB elements (the first loaded into
       // registers before the wait, the next ones from L2, where they were prefetched). No
       // guards: A is zero outside the slice and the rank, x is zero past the slice and nr.
-      const int ok = mbar_wait(ibar, 0) ? 1 : 0;
+      const int ok = mbar_wait(ibar, 0, wlim) ? 1 : 0;
       timed_out = __syncthreads_or(!ok);
       float c0[JPW], c1[JPW];  // two chains per rank row, across the passes
 #pragma unroll
@@ -633,7 +611,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
         }
       }
       if (do_shrink) {
-        const int ok = mbar_wait_cluster(xbar, 0) ? 1 : 0;
+        const int ok = mbar_wait_cluster(xbar, 0, wlim) ? 1 : 0;
         timed_out |= __syncthreads_or(!ok);
         if (!timed_out) {
           for (int e = tid; e < nr * rank; e += NTHREADS) {
@@ -678,8 +656,8 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   // the staged y slice having landed.
   {
     int ok = 1;
-    if (b_staged && !timed_out) ok &= mbar_wait(bbar, 0) ? 1 : 0;
-    if (y_bulk && !timed_out) ok &= mbar_wait(ybar, 0) ? 1 : 0;
+    if (b_staged && !timed_out) ok &= mbar_wait(bbar, 0, wlim) ? 1 : 0;
+    if (y_bulk && !timed_out) ok &= mbar_wait(ybar, 0, wlim) ? 1 : 0;
     timed_out |= __syncthreads_or(!ok);
   }
 
@@ -845,11 +823,14 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
     }
   }
 
-  // Copies still in flight after a time-out land before the CTA exits (bounded waits).
+  // Copies still in flight after a time-out land before the CTA exits (bounded waits), and so do
+  // the peers' pushes into this CTA's exchange buffer (a peer that gave up before pushing never
+  // completes that barrier: the wait then ends at its limit).
   if (timed_out) {
-    if (b_staged) (void)mbar_wait(bbar, 0, 100000000ull);
-    if (x_bulk) (void)mbar_wait(ibar, 0, 100000000ull);
-    if (y_bulk) (void)mbar_wait(ybar, 0, 100000000ull);
+    if (b_staged) (void)mbar_wait(bbar, 0, kDrainLimitNs);
+    if (x_bulk) (void)mbar_wait(ibar, 0, kDrainLimitNs);
+    if (y_bulk) (void)mbar_wait(ybar, 0, kDrainLimitNs);
+    if (clustered && do_shrink) (void)mbar_wait_cluster(xbar, 0, kDrainLimitNs);
     if (tid == 0) report(p.status, MLORA_STATUS_TIMEOUT);
   }
   if (clustered) cluster_wait();  // no CTA leaves while a peer may still write into its shared memory
@@ -859,15 +840,22 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
 template <int DT, int MODE, int RT, int JPW>
 cudaError_t launch_one(const DecodeParams &p, unsigned grid, size_t smem, int cluster, bool pdl, cudaStream_t stream) {
   auto kern = decode_kernel<DT, MODE, RT, JPW>;
-  static int configured_smem[64] = {0};  // per device ordinal
+  // Kernel attributes are per device: the dynamic shared memory this instantiation was set up
+  // for on each device. An entry is raised only after the attribute calls behind it returned,
+  // so a thread that reads it large enough may launch at once.
+  static std::atomic<int> configured_smem[kMaxDevices];
+  static std::mutex mu;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && configured_smem[dev] < (int)smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    configured_smem[dev] = (int)smem;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+  if (dev >= kMaxDevices || configured_smem[dev].load(std::memory_order_acquire) < (int)smem) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= kMaxDevices || configured_smem[dev].load(std::memory_order_relaxed) < (int)smem) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      if (dev < kMaxDevices) configured_smem[dev].store((int)smem, std::memory_order_release);
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);

@@ -1,6 +1,8 @@
 // decode_launch.cu -- host side of the decode kernels: rows per tile, split, stage sizes, grid.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "decode_impl.cuh"
 #include "launch.h"
 
@@ -8,20 +10,26 @@ namespace mlora {
 
 namespace {
 
-int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 64) return 148;
-  if (!cached[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
-  }
-  return cached[dev];
+int query_sm_count(int dev) {
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  return n;
 }
 
 }  // namespace
+
+int sm_count() {
+  static std::atomic<int> cached[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+  if (dev >= kMaxDevices) return query_sm_count(dev);
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {  // concurrent first calls store the same value
+    n = query_sm_count(dev);
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
 
 cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stream, bool pdl, int force_csplit) {
   using decode::Layout;
@@ -38,11 +46,18 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   const bool sgmv = p.seg_off != nullptr;
   const bool multi = sgmv && p.M >= 2 * (p.nseg > 0 ? p.nseg : 1);
   p.rt = multi ? 4 : 1;
-  int64_t tiles = !sgmv ? (int64_t)p.M : (p.rt == 1 ? (int64_t)p.M : (int64_t)p.nseg + (p.M + p.rt - 1) / p.rt);
-  if (sgmv && p.tc_min > 0) {
-    // only segments shorter than tc_min rows are left for these kernels
-    const int64_t per_seg = (p.tc_min - 1 + p.rt - 1) / p.rt;
-    tiles = tiles < (int64_t)p.nseg * per_seg ? tiles : (int64_t)p.nseg * per_seg;
+  const int64_t all_tiles =
+      !sgmv ? (int64_t)p.M : (p.rt == 1 ? (int64_t)p.M : (int64_t)p.nseg + (p.M + p.rt - 1) / p.rt);
+  int64_t tiles = 0;  // the most any problem has (virtual tiles past a problem's own count idle)
+  for (int q = 0; q < p.nprob; ++q) {
+    int64_t tq = all_tiles;
+    const int tcm = p.prob[q].tc_min;
+    if (sgmv && tcm > 0) {
+      // only segments shorter than tc_min rows are left for these kernels
+      const int64_t per_seg = (tcm - 1 + p.rt - 1) / p.rt;
+      tq = tq < (int64_t)p.nseg * per_seg ? tq : (int64_t)p.nseg * per_seg;
+    }
+    tiles = tiles > tq ? tiles : tq;
   }
   if (tiles <= 0) return cudaSuccess;
   p.tiles = (int32_t)tiles;

@@ -27,21 +27,19 @@ struct ProblemDev {
   uint16_t *y;
   int64_t ldy;
   float *v;  // [M][r_max]
+  int32_t tc_min;  // > 0: segments of at least tc_min rows are done by the tensor-core kernels;
+                   // the CUDA-core kernel takes only the shorter segments of this problem
 };
 
 struct DecodeParams {
   ProblemDev prob[MLORA_MAX_GROUP];
   int32_t nprob;
-  PoolDev next_pool[MLORA_MAX_GROUP];  // L2 prefetch hint: pools and layers of the next call
-  int32_t next_layer[MLORA_MAX_GROUP];
-  int32_t nnext;
   const int32_t *seg_off, *seg_slot;  // SGMV (seg_off != nullptr)
   int32_t nseg;
   const int32_t *row_slot;  // BGMV
   int32_t M;
   int32_t *status;
-  int32_t tc_min;  // > 0: segments of at least tc_min rows are done by the tensor-core kernels;
-                   // these kernels take only the shorter segments
+  uint64_t wait_ns;  // limit of the kernel's waits (0 = the default, kWaitLimitNs)
   // chosen by the launcher
   int32_t rt, tiles, csplit, kb, nb, ny, xw, r_alloc;  // nb: staged B columns; ny: y slice staged;
                                                       // xw: x row width staged (whole d_in slice), 0 = one pass
@@ -65,6 +63,12 @@ struct TcParams {
 
 constexpr int kTcMinRows = 32;
 
+// Number of SMs of the current device (cached per device ordinal, safe from any host thread).
+int sm_count();
+constexpr int kMaxDevices = 64;  // devices with a cached entry; others are queried on every call
+
+// Whether an SGMV call over num_rows rows in nseg segments on this pool launches the tensor-core
+// kernels for its long segments (decided on the host, which does not see the segment lengths).
 bool tc_eligible(const PoolDev &pool, int num_rows, int nseg);
 cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stream);
 cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stream);

@@ -24,6 +24,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -42,6 +43,8 @@ constexpr int MAX_STAGES = 12;  // shrink ring depth: as many stages as fit, up 
 constexpr int MAX_EBUF = 8;  // expand pipeline buffers: as many as fit with two CTAs per SM, up to this
 constexpr int NTHREADS = 128;
 constexpr int SCAN_CAP = 512;
+constexpr int kTcBatchRows = 256;  // rows in a batch below which the tensor cores are not tried
+constexpr int kTcAvgRows = 8;      // average rows per segment below which they are not tried
 
 struct TcTile {
   int32_t row0, nr, slot, rank, skip, bad;
@@ -473,7 +476,7 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
       }
       // nothing may land in shared memory after the CTA exits: wait for the last loads (bounded)
       for (int i = max(issued - EBUF, 0); i < issued; ++i)
-        (void)mbar_wait(&full[i % EBUF], (uint32_t)(i / EBUF) & 1u, 100000000ull);
+        (void)mbar_wait(&full[i % EBUF], (uint32_t)(i / EBUF) & 1u, kDrainLimitNs);
     }
     __syncwarp();
   } else if (active && warp == EXP_EPI_WARPS + 1) {
@@ -507,7 +510,7 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
       }
       // every MMA issued so far completes before TMEM is released (bounded)
       tc::mma_commit(mmadone);
-      (void)mbar_wait(mmadone, 0, 100000000ull);
+      (void)mbar_wait(mmadone, 0, kDrainLimitNs);
     }
     __syncwarp();
   } else if (active && warp == EXP_EPI_WARPS + 2) {
@@ -617,16 +620,6 @@ bool encode_2d(CUtensorMap *m, int dtype, const void *base, int64_t cols, int64_
   return r == CUDA_SUCCESS;
 }
 
-int sm_count_tc() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0, v = 0;
-    cudaGetDevice(&dev);
-    n = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 148;
-  }
-  return n;
-}
-
 template <typename K>
 cudaError_t set_smem(K kern, size_t smem) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -637,10 +630,15 @@ cudaError_t set_smem(K kern, size_t smem) {
 // Segments of at least this many rows run on the tensor cores (last block masked).
 constexpr int TC_MIN_ROWS = kTcMinRows;
 
+// The host does not see the segment lengths, only the batch's size: the tensor-core kernels are
+// launched for a batch with enough rows for long segments to be worth two extra launches (at
+// least kTcBatchRows rows, kTcAvgRows per segment on average -- a prefill batch, or prompts mixed
+// with decode rows). They take every segment of at least kTcMinRows rows; the CUDA-core kernel
+// takes the rest. A decode batch (a few rows per segment) runs on the CUDA-core kernel alone.
 bool tc_eligible(const PoolDev &pool, int num_rows, int nseg) {
   return pool.kind == MLORA_POOL_STACKED && (pool.dtype == MLORA_BF16 || pool.dtype == MLORA_FP16) &&
-         pool.r_max <= 128 && num_rows >= BM &&
-         (int64_t)num_rows >= (int64_t)64 * (nseg > 0 ? nseg : 1) && encoder() != nullptr;
+         pool.r_max <= 128 && num_rows >= kTcBatchRows &&
+         (int64_t)num_rows >= (int64_t)kTcAvgRows * (nseg > 0 ? nseg : 1) && encoder() != nullptr;
 }
 
 cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stream) {
@@ -659,7 +657,7 @@ cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stre
   // K split: as many parts as keep the whole grid resident (one wave)
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NTHREADS, smem) != cudaSuccess || occ < 1) occ = 1;
-  int ks = occ * sm_count_tc() / (p.tiles > 0 ? p.tiles : 1);
+  int ks = occ * sm_count() / (p.tiles > 0 ? p.tiles : 1);
   ks = ks < 1 ? 1 : ks > 4 ? 4 : ks;
   ks = ks > kb_total ? kb_total : ks;
   p.ksplit = ks;
@@ -693,7 +691,7 @@ cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stre
   // best on the 13B prefill: 16 blocks of 64 columns per CTA at d_out 5120, ~40 at 13824;
   // shorter runs pay the V setup more often, longer ones leave SMs idle).
   {
-    int runs = 4 * sm_count_tc() / (p.tiles > 0 ? p.tiles : 1);
+    int runs = 4 * sm_count() / (p.tiles > 0 ? p.tiles : 1);
     runs = runs < 1 ? 1 : runs > p.nblk_total ? p.nblk_total : runs;
     p.nper = (p.nblk_total + runs - 1) / runs;
   }

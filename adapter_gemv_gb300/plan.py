@@ -12,19 +12,16 @@ from typing import List, Sequence
 
 import torch
 
-from . import MLORA_MAX_GROUP, Group, lora_set_programmatic_launch, make_pool
+from . import MLORA_MAX_GROUP, CallSequence, Group, make_pool
 
 
 class StepPlan:
-    def __init__(self, ops: Sequence, batch, status=None, programmatic: bool = True, prefetch_next: bool = False):
+    def __init__(self, ops: Sequence, batch, status=None, programmatic: bool = True):
         """ops: objects with .pool .layer .x .y (as workloads.Op); batch: .M .seg_offsets .seg_slot.
-        programmatic: launch every call but the first with programmatic dependent launch. Safe
-        because the kernel before each of those calls is this library's previous call, which
-        writes none of the inputs a call reads before its wait (metadata, pool). The first call
-        keeps an ordinary dependency on whatever ran before the step.
-        prefetch_next: each call carries the next call's problems as an L2 prefetch hint. Off by
-        default: on a decode step the hint's extra traffic is issued while each call's own adapter
-        rows are in flight and slows the step down (about 3% on the Llama-2-7B bs32 step)."""
+        programmatic: launch every call but the first with programmatic dependent launch (a flag
+        of that call alone). Safe because the kernel before each of those calls is this library's
+        previous call, which writes none of the inputs a call reads before its wait (metadata,
+        pool). The first call keeps an ordinary dependency on whatever ran before the step."""
         self.programmatic = programmatic
         self.handles = {}
         groups: List[List] = []
@@ -47,21 +44,20 @@ class StepPlan:
                 h = self.handles.setdefault(id(op.pool), make_pool(op.pool))
                 v = self.scratch[q].view(-1)[:batch.M * op.pool.r_max].view(batch.M, op.pool.r_max)  # row stride r_max
                 probs.append((op.y, op.x, h, op.layer, v))
-            self.calls.append(Group(probs, batch.seg_offsets, batch.seg_slot, batch.M, status))
-        if prefetch_next:
-            for a, b in zip(self.calls, self.calls[1:]):
-                a.set_next(b)  # each call prefetches the next call's adapter rows into L2
+            self.calls.append(Group(probs, batch.seg_offsets, batch.seg_slot, batch.M, status,
+                                    programmatic=programmatic and len(self.calls) > 0))
         self.groups = groups
+        # the whole step as one call into the library (the same launches as the calls above)
+        self.sequence = CallSequence(self.calls, programmatic, status)
 
     def __call__(self, stream=None):
-        prev = lora_set_programmatic_launch(False)
-        try:
-            for q, c in enumerate(self.calls):
-                if q == 1:
-                    lora_set_programmatic_launch(self.programmatic)
-                c(stream)
-        finally:
-            lora_set_programmatic_launch(prev)
+        """Issue the step: one lora_sgmv_sequence call (every grouped call, launched natively)."""
+        self.sequence(stream)
+
+    def call_one_by_one(self, stream=None):
+        """Issue the step as one lora_sgmv_grouped_ex call per group (the same launches)."""
+        for c in self.calls:
+            c(stream)
 
     @property
     def launches(self) -> int:

@@ -10,7 +10,8 @@ o, gate/up, down per layer) through the C ABI and replayed as a CUDA graph.
   value     rows/s with every input resident in HBM (2.8 GB of algorithmic traffic per step,
             far above the 129 MB L2, so no flush is needed between steps)
   e2e       the same metric with the step's inputs (x, base y) copied from pinned host memory
-            and the result y copied back inside the timed region
+            and the result y copied back inside the timed region, each step issued by one call
+            into the library (e2e.graph: the same with the step replayed as a CUDA graph)
   roofline  algorithmic bytes of the step's launches / their time, against the measured HBM copy
             bandwidth (MEASURED_PEAKS.json)
   cpu_baseline / --impl reference: the fp64 oracle on the host cores, on a bounded sample of the
@@ -177,26 +178,100 @@ def ncu_traffic(kernel: str, workload_key: str):
 # the headline step
 
 
-def build_step(dev, dist="distinct"):
-    import adapter_gemv_gb300 as m
-    from adapter_gemv_gb300.plan import StepPlan
-    w = W.sgmv_decode_7b(device=dev, dist=dist)
-    # re-home every base y of the step into one flat buffer (one copy in / one copy out for e2e)
-    total = sum(op.y.numel() for op in w.ops)
-    ybuf = torch.empty(total, dtype=w.dtype, device=dev)
-    o = 0
-    for op in w.ops:
-        n = op.y.numel()
-        ybuf[o:o + n].view_as(op.y).copy_(op.y)
-        op.y = ybuf[o:o + n].view(op.y.shape)
-        o += n
+def io_set(w, dev):
+    """The step's activations (every distinct x) and base outputs (every y) re-homed into two flat
+    device buffers, with ops that point at them: one host-to-device copy of each buffer brings a
+    whole step's inputs in, one device-to-host copy of the y buffer takes its result out."""
     xs = []
     for op in w.ops:
         if all(op.x.data_ptr() != x.data_ptr() for x in xs):
             xs.append(op.x)
+    xbuf = torch.empty(sum(x.numel() for x in xs), dtype=w.dtype, device=dev)
+    ybuf = torch.empty(sum(op.y.numel() for op in w.ops), dtype=w.dtype, device=dev)
+    xview, o = {}, 0
+    for x in xs:
+        v = xbuf[o:o + x.numel()].view(x.shape)
+        v.copy_(x)
+        xview[x.data_ptr()] = v
+        o += x.numel()
+    ops, o = [], 0
+    for op in w.ops:
+        v = ybuf[o:o + op.y.numel()].view(op.y.shape)
+        v.copy_(op.y)
+        ops.append(W.Op(op.name, op.pool, op.layer, xview[op.x.data_ptr()], v))
+        o += op.y.numel()
+    return ops, xbuf, ybuf
+
+
+def build_step(dev, dist="distinct"):
+    import adapter_gemv_gb300 as m
+    from adapter_gemv_gb300.plan import StepPlan
+    w = W.sgmv_decode_7b(device=dev, dist=dist)
+    w.ops, xbuf, ybuf = io_set(w, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     plan = StepPlan(w.ops, w.batch, status)
-    return w, plan, ybuf, xs, status, m
+    return w, plan, ybuf, xbuf, status, m
+
+
+def e2e_pipeline(plans, graphs, xbufs, ybufs, steps, dev, use_graphs):
+    """End-to-end time of `steps` decode steps with host buffers: step k's activations and base
+    outputs are copied in from pinned host memory and its result copied back, every step. Three
+    device buffer sets rotate, so step k+1's input copy and step k-1's output copy run on their
+    own streams while step k computes (the copies are inside the timed region; they only overlap
+    with compute). Step k is issued through the library's public API: one lora_sgmv_sequence call
+    (use_graphs False) or a replay of a CUDA graph captured from it (use_graphs True).
+    Returns (seconds, h2d bytes per step, d2h bytes per step)."""
+    n = len(plans)
+    comp, cin, cout = (torch.cuda.Stream(device=dev) for _ in range(3))
+    host_x = torch.empty(xbufs[0].shape, dtype=xbufs[0].dtype, pin_memory=True)
+    host_y = torch.empty(ybufs[0].shape, dtype=ybufs[0].dtype, pin_memory=True)
+    host_x.copy_(xbufs[0])
+    host_y.copy_(ybufs[0])
+    host_out = [torch.empty(host_y.shape, dtype=host_y.dtype, pin_memory=True) for _ in range(n)]
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_comp = [torch.cuda.Event() for _ in range(n)]
+    ev_out = [torch.cuda.Event() for _ in range(n)]
+    torch.cuda.synchronize()
+
+    def copy_in(k):
+        b = k % n
+        cin.wait_event(ev_out[b])  # the buffer's previous result has been copied out
+        with torch.cuda.stream(cin):
+            xbufs[b].copy_(host_x, non_blocking=True)
+            ybufs[b].copy_(host_y, non_blocking=True)
+        ev_in[b].record(cin)
+
+    def run(steps_, start=None, end=None):
+        if start is not None:
+            start.record(cin)
+        copy_in(0)
+        for k in range(steps_):
+            b = k % n
+            if k + 1 < steps_:
+                copy_in(k + 1)
+            comp.wait_event(ev_in[b])
+            if use_graphs:
+                with torch.cuda.stream(comp):
+                    graphs[b].replay()
+            else:
+                plans[b](comp)
+            ev_comp[b].record(comp)
+            cout.wait_event(ev_comp[b])
+            with torch.cuda.stream(cout):
+                host_out[b].copy_(ybufs[b], non_blocking=True)
+            ev_out[b].record(cout)
+        if end is not None:
+            end.record(cout)
+
+    run(2 * n)  # warm-up
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run(steps, start, end)
+    end.synchronize()
+    torch.cuda.synchronize()
+    h2d = xbufs[0].numel() * xbufs[0].element_size() + ybufs[0].numel() * ybufs[0].element_size()
+    d2h = ybufs[0].numel() * ybufs[0].element_size()
+    return start.elapsed_time(end) / 1e3, h2d, d2h
 
 
 def step_bytes(w):
@@ -423,7 +498,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev)
     hbm, peak_kind = peaks()
 
-    w, plan, ybuf, xs, status, m = build_step(dev, "distinct")
+    w, plan, ybuf, xbuf, status, m = build_step(dev, "distinct")
     rows = w.batch.M
     bytes_step = step_bytes(w)
     g = capture(plan, stream)
@@ -447,32 +522,23 @@ def run_ours(args):
     ms = secs / args.steps * 1e3
     value = job_rows_per_s(ws, rows, args.steps, secs)
 
-    # e2e: pinned host inputs -> device, the step, result back to the host, every step
-    host_y = torch.empty(ybuf.shape, dtype=ybuf.dtype, pin_memory=True)
-    host_y.copy_(ybuf)
-    host_out = torch.empty_like(host_y, pin_memory=True)
-    host_x = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x) for x in xs]
+    # e2e: pinned host inputs -> device, the step, result back to the host, every step; three
+    # buffer sets so the copies of the neighbouring steps overlap this step's compute
+    from adapter_gemv_gb300.plan import StepPlan
+    plans, graphs, xbufs, ybufs = [plan], [g], [xbuf], [ybuf]
+    for _ in range(2):
+        ops_k, xb_k, yb_k = io_set(w, dev)
+        p_k = StepPlan(ops_k, w.batch, status)
+        plans.append(p_k)
+        graphs.append(capture(p_k, stream))
+        xbufs.append(xb_k)
+        ybufs.append(yb_k)
     e2e_steps = max(3, min(args.steps, 200))
-    with torch.cuda.stream(stream):
-        def e2e_once():
-            ybuf.copy_(host_y, non_blocking=True)
-            for hx, x in zip(host_x, xs):
-                x.copy_(hx, non_blocking=True)
-            g.replay()
-            host_out.copy_(ybuf, non_blocking=True)
-        for _ in range(2):
-            e2e_once()
-        barrier()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_once()
-        ev1.record(stream)
-        ev1.synchronize()
-    e2e_secs = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, dev)
-    h2d = ybuf.numel() * ybuf.element_size() + sum(x.numel() * x.element_size() for x in xs)
-    d2h = ybuf.numel() * ybuf.element_size()
-
+    e2e_secs, h2d, d2h = e2e_pipeline(plans, graphs, xbufs, ybufs, e2e_steps, dev, use_graphs=False)
+    e2e_secs = max_over_ranks(e2e_secs, dev)
+    e2e_g_secs, _, _ = e2e_pipeline(plans, graphs, xbufs, ybufs, e2e_steps, dev, use_graphs=True)
+    e2e_g_secs = max_over_ranks(e2e_g_secs, dev)
+    del plans, graphs, xbufs, ybufs
     if rank != 0:
         if ws > 1:
             torch.distributed.destroy_process_group()
@@ -494,7 +560,12 @@ def run_ours(args):
                      "traffic": ncu_traffic("decode_kernel_fused", "decode7b_distinct")},
         "e2e": {"value": round(job_rows_per_s(ws, rows, e2e_steps, e2e_secs), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_secs / e2e_steps * 1e3, 4),
-                "api": "lora_sgmv_grouped via the Python binding, replayed as a CUDA graph; pinned host buffers"},
+                "api": f"one lora_sgmv_sequence call per step (its {plan.launches} grouped calls issued by the "
+                       "library, no CUDA graph); x and base y copied in from pinned host memory and y copied "
+                       "out every step, the copies of the next and previous steps overlapping this step's compute",
+                "graph": {"value": round(job_rows_per_s(ws, rows, e2e_steps, e2e_g_secs), 1),
+                          "ms_per_step": round(e2e_g_secs / e2e_steps * 1e3, 4),
+                          "api": "the same, each step a replay of a CUDA graph captured from that call"}},
         "gpu_launches": plan.launches * args.steps,
         "clocks": sampler.summary() if sampler else None,
     }

@@ -205,32 +205,56 @@ MLORA_API int lora_sgmv_grouped(const mlora_problem *problems, int32_t num_probl
                       const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t *dev_status,
                       void *stream);
 
-/* Same as lora_sgmv_grouped, plus a prefetch hint for a sequence of grouped calls over one batch
- * (a decode step): `next` [num_next] lists the problems of the call that will follow on this
- * stream, over the same rows and segments. While this call runs, its CTAs request into L2 the
- * adapter rows (A and B of each row's slot) that those problems will read, so that the next
- * call's weights stream from HBM during this one. Only the pools and layers of `next` are read;
- * nothing is written for them and the result of this call does not depend on the hint
- * (num_next == 0 makes it lora_sgmv_grouped). (No counterpart on the pages: an L2 prefetch
- * schedule for GB300's 129 MB L2.) */
-MLORA_API int lora_sgmv_grouped_prefetch(const mlora_problem *problems, int32_t num_problems,
-                                         const mlora_problem *next, int32_t num_next, const int32_t *seg_offsets,
-                                         const int32_t *seg_slot, int32_t num_segments, int32_t num_rows,
-                                         int32_t *dev_status, void *stream);
+/* Launch flags of lora_sgmv_grouped_ex. */
+#define MLORA_LAUNCH_PROGRAMMATIC 1u /* programmatic dependent launch for this call (see below) */
+
+/* lora_sgmv_grouped with launch flags given per call instead of taken from the calling thread's
+ * setting (lora_set_programmatic_launch). flags: 0 or MLORA_LAUNCH_PROGRAMMATIC; other bits are
+ * rejected with MLORA_ERR_SHAPE. (No counterpart on the pages: a launch-latency measure for
+ * GB300.) */
+MLORA_API int lora_sgmv_grouped_ex(const mlora_problem *problems, int32_t num_problems, const int32_t *seg_offsets,
+                                   const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, uint32_t flags,
+                                   int32_t *dev_status, void *stream);
+
+/* ---- sequence form: the grouped calls of a whole step in one call ------------------------
+ * A decoder step issues one grouped call per dependent stage of every layer (q,k,v; o;
+ * gate,up; down for a Llama layer: 4 x num_layers calls). lora_sgmv_sequence issues such a
+ * list of grouped calls, in order, on `stream`, from native code: the same launches as
+ * num_groups calls of lora_sgmv_grouped_ex, for one call's host cost. Every group is validated
+ * before anything is launched (a host-detectable error in any group returns its code and
+ * launches nothing). flags: MLORA_LAUNCH_PROGRAMMATIC gives every call after the first
+ * programmatic dependent launch (the first keeps an ordinary dependency on whatever ran
+ * before); the groups then must not write each other's metadata or pools, which this
+ * library's calls never do. Each group's problems must not write the x of a later group
+ * while that group may read it -- as in a real step, where x of the next stage comes from
+ * other kernels. (No counterpart on the pages: Punica issues 7 x L launches per step from
+ * the host; this is the same schedule issued natively.) */
+typedef struct {
+  const mlora_problem *problems; /* host array of num_problems entries */
+  int32_t num_problems;          /* 1 .. MLORA_MAX_GROUP */
+  const int32_t *seg_offsets;    /* device [num_segments + 1] */
+  const int32_t *seg_slot;       /* device [num_segments] */
+  int32_t num_segments;
+  int32_t num_rows;
+} mlora_group;
+
+MLORA_API int lora_sgmv_sequence(const mlora_group *groups, int32_t num_groups, uint32_t flags, int32_t *dev_status,
+                                 void *stream);
 
 /* ---- utilities --------------------------------------------------------------------------- */
 
 /* Static text for a return code; for MLORA_ERR_CUDA it names the last CUDA error this thread saw. */
 MLORA_API const char *lora_error_string(int code);
 
-/* Programmatic dependent launch (off by default). When on, every later call launches its
- * kernel so that it may start while the previous kernel in the stream is still running: before
- * waiting for that kernel it reads only its rows' metadata (offsets, slots), the pool descriptor
- * arrays (rank, scale, page tables) and the adapter weights, and it requests the weights; x, y
- * and v are touched only after the wait. Turn it on only where the kernel launched just before
- * each call does not write those inputs -- e.g. a sequence of this library's calls, or calls
- * whose inputs were written by copies or at least one kernel earlier. Process-wide; returns
- * the previous setting. (No counterpart on the pages: a launch-latency measure for GB300.) */
+/* Programmatic dependent launch (off by default), for the calling host thread. When on, every
+ * later call from this thread launches its kernels so that they may start while the previous
+ * kernel in the stream is still running: before waiting for that kernel a kernel reads only its
+ * rows' metadata (offsets, slots), the pool descriptor arrays (rank, scale, page tables) and the
+ * adapter weights, and it requests the weights; x, y, v and dev_status are touched only after
+ * the wait. Turn it on only where the kernel launched just before each call does not write those
+ * inputs -- e.g. a sequence of this library's calls, or calls whose inputs were written by copies
+ * or at least one kernel earlier. Other host threads keep their own setting. Returns this
+ * thread's previous setting. (No counterpart on the pages: a launch-latency measure for GB300.) */
 MLORA_API int lora_set_programmatic_launch(int enable);
 
 /* MLORA_ABI_VERSION of the loaded library. */
@@ -238,6 +262,15 @@ MLORA_API int lora_abi_version(void);
 
 /* Number of kernel launches the library has issued from this process (all threads). */
 MLORA_API int64_t lora_launch_count(void);
+
+/* Testing hook for the time-out path: limit, in nanoseconds, of the waits inside the CUDA-core
+ * kernels launched later by the calling thread (the waits for their own bulk copies and for
+ * their cluster peers' partial sums). 0 restores the default of 2 s. With a limit of a few
+ * nanoseconds a wait gives up unless its data has already landed, the kernel sets
+ * MLORA_STATUS_TIMEOUT and skips the work that needed the data, and copies still in flight are
+ * drained (with the default limit) before the kernel exits. Not for production use: results of
+ * rows whose waits gave up are left unwritten. (No counterpart on the pages.) */
+MLORA_API void lora_test_set_wait_limit_ns(uint64_t limit_ns);
 
 #ifdef __cplusplus
 }

@@ -133,6 +133,21 @@ def test_grouped_limits(L):
         arr[q].y, arr[q].ldy, arr[q].x, arr[q].ldx, arr[q].v_scratch = Y, 64, X, 64, V
         arr[q].pool = ctypes.pointer(p)
     assert L.lora_sgmv_grouped(arr, 2, OFF, SLOT, 1, 8, None, None) == m.ERR_DTYPE
+    assert L.lora_sgmv_grouped_ex(arr, 2, OFF, SLOT, 1, 8, m.LAUNCH_PROGRAMMATIC, None, None) == m.ERR_DTYPE
+    # unknown launch flags are refused before anything else is looked at
+    assert L.lora_sgmv_grouped_ex(arr, 1, OFF, SLOT, 1, 8, 2, None, None) == m.ERR_SHAPE
+
+
+def test_programmatic_launch_setting_is_per_thread(L):
+    """lora_set_programmatic_launch changes the calling thread's setting only."""
+    import threading
+    assert L.lora_set_programmatic_launch(1) == 0
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(L.lora_set_programmatic_launch(0)))
+    t.start()
+    t.join()
+    assert seen == [0], "a new thread inherited another thread's setting"
+    assert L.lora_set_programmatic_launch(0) == 1
 
 
 def test_binding_refuses_cpu_tensors():

@@ -30,7 +30,8 @@ def c_layout(tmp_path, struct, fields):
     return {name: (int(a), int(b)) for name, a, b in (ln.split() for ln in out if ln)}
 
 
-@pytest.mark.parametrize("struct, cls", [("mlora_pool", m.mlora_pool), ("mlora_problem", m.mlora_problem)])
+@pytest.mark.parametrize("struct, cls", [("mlora_pool", m.mlora_pool), ("mlora_problem", m.mlora_problem),
+                                         ("mlora_group", m.mlora_group)])
 def test_struct_layouts_match(tmp_path, struct, cls):
     names = [f for f, _ in cls._fields_]
     c = c_layout(tmp_path, struct, names)
@@ -52,7 +53,7 @@ def width(c_arg: str):
     """'p' for any pointer, else the integer width in bits."""
     if "*" in c_arg:
         return "p"
-    for t, w in (("int64_t", 64), ("int32_t", 32), ("int ", 32), ("size_t", 64)):
+    for t, w in (("int64_t", 64), ("int32_t", 32), ("uint32_t", 32), ("uint64_t", 64), ("int ", 32), ("size_t", 64)):
         if c_arg.startswith(t):
             return w
     raise AssertionError(f"unhandled C argument type: {c_arg}")

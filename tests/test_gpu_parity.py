@@ -67,20 +67,6 @@ def test_decode_step_7b_as_benched(dev, dist):
             check_op(op, w.batch, "sgmv", op.y, y_before=before[id(op)], what=f"{dist} {op.name} L{op.layer}")
 
 
-def test_decode_step_with_next_call_prefetch(dev):
-    """The same step with every call carrying the next call's problems as an L2 prefetch hint
-    (lora_sgmv_grouped_prefetch): the hint changes no result."""
-    w = W.sgmv_decode_7b(device=dev, dist="skewed", num_layers=3, layers=[0, 1, 2])
-    st = status_of(dev)
-    before = {id(op): bits(op.y) for op in w.ops}
-    plan = StepPlan(w.ops, w.batch, st, prefetch_next=True)
-    plan()
-    torch.cuda.synchronize()
-    assert st.item() == 0
-    for op in w.ops:
-        check_op(op, w.batch, "sgmv", op.y, y_before=before[id(op)], what=f"prefetch {op.name} L{op.layer}")
-
-
 def ragged_rank16_step(dev, dtype, seed):
     """Chained one-row problems whose pools have r_max 16 (the kernel that stages A in shared
     memory): ranks 4/8/13/16 (padding rows hold NaN), d_in slices that end inside a pass of A

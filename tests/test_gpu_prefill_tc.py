@@ -33,8 +33,10 @@ CASES = [
     (128, [128, 96], 1032, 1104, [256, 131], [0, 1]),
     # segments around the 32-row threshold: partial tensor-core tiles next to CUDA-core segments
     (16, [16, 5, 16], 320, 328, [31, 32, 33, 64, 127, 200, 1], [0, 1, 2, 0, 1, 2, -1]),
-    # enough 128-row blocks that the K split is 3 (rows do not divide evenly over the cluster)
+    # many 128-row blocks: one CTA per block, no K split
     (16, [16, 16], 256, 136, [128 * 60 + 7, 128 * 41], [0, 1]),
+    # few blocks: K split over a cluster of 4 (5120 / 128 K blocks do not divide evenly)
+    (64, [64, 40], 5120, 264, [384, 131, 2], [0, 1, 1]),
 ]
 
 
@@ -112,3 +114,52 @@ def test_prefill_bad_offsets_launch_tc_but_write_nothing(dev):
     torch.cuda.synchronize()
     assert st.item() == m.STATUS_BAD_OFFSETS
     assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+
+
+def mixed_batch(dev, dtype, seed, d_in, d_out, r_max=16):
+    """Punica's batch layout: the prompts of new requests first (one segment and adapter each),
+    then one-row decode segments (an adapter per request, some sharing a prompt's adapter, some
+    without adapter)."""
+    rng = np.random.default_rng(seed)
+    g = W.generator(seed, dev)
+    prompts = [300, 1200, 2000]
+    num_slots = 40
+    ranks = rng.integers(1, r_max + 1, num_slots).astype(np.int32)
+    pool = W.stacked_pool(num_slots=num_slots, num_layers=1, r_max=r_max, d_in=d_in, d_out=d_out, dtype=dtype,
+                          gen=g, device=dev, ranks=ranks)
+    decode_slots = rng.integers(-1, num_slots, 64)
+    decode_slots[:3] = [0, 1, 2]  # the prompts' adapters again, in decode rows
+    lens = np.r_[prompts, np.ones(64, np.int64)]
+    slots = np.r_[[0, 1, 2], decode_slots].astype(np.int32)
+    batch = W.batch_from_segments(lens, slots).to(dev)
+    x = W.normal((batch.M, d_in), 1.0, dtype, g, dev)
+    y = W.uniform((batch.M, d_out), -1, 1, dtype, g, dev)
+    return pool, batch, x, y
+
+
+@pytest.mark.parametrize("form", ["two_phase", "fused", "grouped"])
+def test_mixed_prefill_and_decode_batch(dev, form):
+    """Three prompts of 300-2000 rows and 64 one-row decode segments in one SGMV batch: the
+    prompts run on the tensor-core kernels, the decode rows on the CUDA-core kernel, and every
+    row matches the oracle."""
+    pool, batch, x, y0 = mixed_batch(dev, torch.bfloat16, 17, 1024, 1032)
+    h = m.make_pool(pool)
+    M = batch.M
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    before = m.launch_count()
+    if form == "grouped":
+        ys = [y0.clone(), y0.clone()]
+        m.lora_sgmv_grouped([(ys[q], x, h, 0, new_v(M, 16, dev)) for q in range(2)], batch.seg_offsets,
+                            batch.seg_slot, st)
+        launches, outs, v = 2 * 2 + 1, ys, None
+    else:
+        op = W.Op("mixed", pool, 0, x, y0)
+        y, v = run_tc(dev, op, batch, form, 16)
+        launches, outs = 0, [y]
+    torch.cuda.synchronize()
+    if form == "grouped":
+        assert m.launch_count() - before == launches, "the grouped call did not use the tensor-core kernels"
+    assert st.item() == 0
+    op = W.Op("mixed", pool, 0, x, y0)
+    for y in outs:
+        check_op(op, batch, "sgmv", y, v if form == "two_phase" else None, what=f"mixed batch {form}")

@@ -17,7 +17,7 @@ import torch
 
 import adapter_gemv_gb300 as m
 import workloads as W
-from gpu_util import TOL, bits
+from gpu_util import TOL, bits, check_op
 
 pytestmark = pytest.mark.gpu
 
@@ -72,6 +72,10 @@ def test_noalloc_matches_lora_sgmv_on_two_calls_in_a_row(dev):
         y_ref, y_na = run_both(dev, pool, batch, x, y)
         assert not np.array_equal(bits(y_na), bits(y)), "the call changed nothing"
         assert_within_tolerance(y_na, y_ref)
+        # the same kernels with the same split run in both calls: the bits agree too
+        assert np.array_equal(bits(y_na), bits(y_ref)), "lora_sgmv_noalloc and lora_sgmv differ in their bits"
+        # and both agree with the fp64 oracle on every row
+        check_op(W.Op("noalloc", pool, 0, x, y), batch, "sgmv", y_na, what="lora_sgmv_noalloc")
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch(dev):

@@ -322,8 +322,9 @@ def sgmv_decode_7b(device="cpu", seed=3, dist="distinct", M=32, num_layers=32, r
                    projections: Sequence[Projection] = LLAMA2_7B, layers: Optional[Sequence[int]] = None) -> Workload:
     """bf16 decode step: all seven Llama-2-7B projections of every layer, r = 16, 32 slots,
     one stacked pool per projection [32 slots][32 layers][16][d]. Slots per row from `dist`;
-    rows grouped into segments (the batch layout), reused by every op of the step. q/k/v/gate/up
-    read one shared x [M][4096]; o reads its own [M][4096]; down reads [M][11008]."""
+    rows grouped into segments (the batch layout), reused by every op of the step. Every layer
+    has its own activations, as in a real step: q/k/v/gate/up of a layer read one x [M][4096]
+    (the normalised hidden state), o reads its own [M][4096], down reads [M][11008]."""
     g = generator(seed, device)
     rng = np.random.default_rng(seed)
     dt = torch.bfloat16
@@ -334,11 +335,11 @@ def sgmv_decode_7b(device="cpu", seed=3, dist="distinct", M=32, num_layers=32, r
     pools = {p.name: stacked_pool(num_slots=num_slots, num_layers=num_layers, r_max=r, d_in=p.d_in, d_out=p.d_out,
                                   dtype=dt, gen=g, device=device) for p in projections}
     hidden = projections[0].d_in
-    x_shared = normal((M, hidden), 1.0, dt, g, device)
-    x_o = normal((M, hidden), 1.0, dt, g, device)
-    x_down = {p.name: normal((M, p.d_in), 1.0, dt, g, device) for p in projections if p.name == "down"}
     ops = []
     for layer in (range(num_layers) if layers is None else layers):
+        x_shared = normal((M, hidden), 1.0, dt, g, device)
+        x_o = normal((M, hidden), 1.0, dt, g, device)
+        x_down = {p.name: normal((M, p.d_in), 1.0, dt, g, device) for p in projections if p.name == "down"}
         for p in projections:
             x = x_o if p.name == "o" else x_down[p.name] if p.name == "down" else x_shared
             y = uniform((M, p.d_out), -1, 1, dt, g, device)
