@@ -29,8 +29,11 @@
 //     the stream start at once. Before griddepcontrol.wait a CTA only reads what no kernel of
 //     this library writes (the rows' metadata, the pool, the page tables); x, y and v, which the
 //     previous kernel may have written, are read after the wait (they may be prefetched into L2
-//     before it). A CTA arrives at its cluster's second barrier as soon as its exchange is done,
-//     so it can leave without waiting for its peers' expand and free its SM for the next launch.
+//     before it).
+//   * One cluster barrier phase only: every CTA arrives at start and waits before pushing (so
+//     every peer's exchange barrier is initialised). No barrier at exit: a CTA leaves once its
+//     own exchange barrier has counted every push into its shared memory, without waiting for
+//     its peers' expand, and frees its SM for the next launch sooner.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -626,10 +629,8 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
           }
         }
       }
-      // Second cluster phase: every push into this CTA has landed (or the wait gave up), so it
-      // needs nothing more from its peers. A CTA leaves only after all peers have arrived, i.e.
-      // after every push in the cluster has landed; the early arrival spares the wait at exit.
-      cluster_arrive_release();
+      // Every push into this CTA has landed (or the wait gave up, and the exit drains it): the
+      // CTA needs nothing more from its peers and its shared memory is no longer written by them.
     } else if (do_shrink && !timed_out && lane == 0) {
 #pragma unroll
       for (int jj = 0; jj < JPW; ++jj) {
@@ -833,7 +834,6 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
     if (clustered && do_shrink) (void)mbar_wait_cluster(xbar, 0, kDrainLimitNs);
     if (tid == 0) report(p.status, MLORA_STATUS_TIMEOUT);
   }
-  if (clustered) cluster_wait();  // no CTA leaves while a peer may still write into its shared memory
 }
 
 // Host: launch one instantiation with the cluster and PDL attributes.
