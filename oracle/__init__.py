@@ -7,7 +7,8 @@ nothing from the CUDA library or its binding.
 The arithmetic lives in ``mlora_oracle.c`` (plain C, fp64, one rounding to the I/O type),
 which follows Punica section 3.4 "The SGMV Operator" (shrink v = x·A, expand y += v·B),
 the reference loop of "Multi-LoRA Serving, in depth" (slot per row, -1 = no adapter,
-per-slot scale) and S-LoRA "Unified Paging" (one page per rank-row of A^T and of B).
+per-slot scale) and S-LoRA "Unified Paging" (a page is one H-vector; a rank-row of A^T or B
+longer than a page spans consecutive entries of the page table).
 This module only marshals numpy arrays into that code; it does no arithmetic of its own.
 
 Every function here is pinned by ``tests/test_oracle_pins.py``; ``tests/test_oracle_mutants.py``
@@ -78,7 +79,8 @@ class Pool:
 
     Stacked: ``a_t`` [num_slots][num_layers][r_max][d_in] and ``b`` [...][r_max][d_out], both
     uint16 bit patterns of the I/O type. Paged: ``pages`` [num_pages][page_elems] and two page
-    tables [num_slots][num_layers][r_max] (int32). ``rank`` int32 [num_slots], ``scale`` float32.
+    tables [num_slots][num_layers][r_max][ceil(d / page_elems)] (int32; d = d_in for A, d_out for
+    B: a vector longer than a page spans several). ``rank`` int32 [num_slots], ``scale`` float32.
     """
 
     def __init__(self, *, dtype, num_slots, num_layers, r_max, d_in, d_out, rank, scale,
@@ -99,8 +101,10 @@ class Pool:
             assert self.b.size == num_slots * num_layers * r_max * d_out
         else:
             assert self.pages.ndim == 2
-            assert self.a_page_table.size == num_slots * num_layers * r_max
-            assert self.b_page_table.size == num_slots * num_layers * r_max
+            pe = self.pages.shape[1]
+            # one entry per page of each vector: ceil(d / page_elems) pages per vector
+            assert self.a_page_table.size == num_slots * num_layers * r_max * (-(-d_in // pe))
+            assert self.b_page_table.size == num_slots * num_layers * r_max * (-(-d_out // pe))
         assert self.rank.size == num_slots and self.scale.size == num_slots
         self._s = _PoolStruct(
             self.kind, self.dtype, self.num_slots, self.num_layers, self.r_max, self.d_in, self.d_out,

@@ -30,15 +30,20 @@
  *                 Punica's LoraWeight.wa "[num_layers, r, in_features]", zh-TW digest 5.4)
  *                 B   [num_slots][num_layers][r_max][d_out]  (row-major B, LoraWeight.wb)
  *   paged pool    S-LoRA (arXiv 2311.03285) "Unified Paging": a page is one vector of
- *                 page_elems elements; A of rank R is R pages (its columns), B is R pages
- *                 (its rows). Page ids come from [num_slots][num_layers][r_max] tables.
+ *                 page_elems elements (one H-vector); A of rank R is R columns, B is R rows,
+ *                 each a vector of d_in (A) or d_out (B) elements stored in pages. A vector
+ *                 longer than a page (page_elems < d, e.g. the 13824-long rows of an MLP
+ *                 projection in pages of hidden size 5120) spans ceil(d / page_elems) pages:
+ *                 the page tables are [num_slots][num_layers][r_max][ceil(d / page_elems)],
+ *                 and element k of a vector is element k % page_elems of the vector's
+ *                 (k / page_elems)-th page. With page_elems >= d every vector is one page.
  *
  * Metadata the pages do not define (everything but slot -1) is reported with status bits
  * and the affected rows are left untouched:
  *   ORC_BAD_OFFSETS  SGMV offsets not 0 = off[0] <= ... <= off[n] = M; nothing is computed.
  *   ORC_BAD_SLOT     slot < -1 or slot >= num_slots.
  *   ORC_BAD_RANK     rank[s] outside [1, r_max].
- *   ORC_BAD_PAGE     a page id (for j < rank[s]) outside [0, num_pages).
+ *   ORC_BAD_PAGE     a page id (of a vector j < rank[s]) outside [0, num_pages).
  */
 #include <math.h>
 #include <stdint.h>
@@ -64,8 +69,8 @@ typedef struct {
   const uint16_t *b; /* stacked B */
   const uint16_t *pages; /* paged: [num_pages][page_elems] */
   int32_t page_elems, num_pages;
-  const int32_t *a_page_table; /* paged: [num_slots][num_layers][r_max] */
-  const int32_t *b_page_table;
+  const int32_t *a_page_table; /* paged: [num_slots][num_layers][r_max][ceil(d_in / page_elems)] */
+  const int32_t *b_page_table; /* paged: [num_slots][num_layers][r_max][ceil(d_out / page_elems)] */
   const int32_t *rank; /* [num_slots] */
   const float *scale; /* [num_slots] */
 } orc_pool;
@@ -158,14 +163,23 @@ static size_t table_index(const orc_pool *p, int s, int layer, int j) {
   return ((size_t)s * (size_t)p->num_layers + (size_t)layer) * (size_t)p->r_max + (size_t)j;
 }
 
+/* Pages one vector of d elements spans (paged pools). */
+static int pages_per_vector(const orc_pool *p, int d) { return (d + p->page_elems - 1) / p->page_elems; }
+
+/* Page table entry of element k of vector j (paged pools): the vector's pages are consecutive
+ * entries, element k sits in its (k / page_elems)-th page. */
+static size_t page_entry(const orc_pool *p, int s, int layer, int j, int d, int k) {
+  return table_index(p, s, layer, j) * (size_t)pages_per_vector(p, d) + (size_t)(k / p->page_elems);
+}
+
 /* A_s[k][j] of the given layer (A is d_in x rank). */
 static double elem_a(const orc_pool *p, int s, int layer, int k, int j) {
   if (p->kind == ORC_POOL_STACKED) {
     size_t row = table_index(p, s, layer, j);
     return orc_decode(p->a_t[row * (size_t)p->d_in + (size_t)k], p->dtype);
   }
-  int32_t page = p->a_page_table[table_index(p, s, layer, j)];
-  return orc_decode(p->pages[(size_t)page * (size_t)p->page_elems + (size_t)k], p->dtype);
+  int32_t page = p->a_page_table[page_entry(p, s, layer, j, p->d_in, k)];
+  return orc_decode(p->pages[(size_t)page * (size_t)p->page_elems + (size_t)(k % p->page_elems)], p->dtype);
 }
 
 /* B_s[j][n] of the given layer (B is rank x d_out). */
@@ -174,8 +188,8 @@ static double elem_b(const orc_pool *p, int s, int layer, int j, int n) {
     size_t row = table_index(p, s, layer, j);
     return orc_decode(p->b[row * (size_t)p->d_out + (size_t)n], p->dtype);
   }
-  int32_t page = p->b_page_table[table_index(p, s, layer, j)];
-  return orc_decode(p->pages[(size_t)page * (size_t)p->page_elems + (size_t)n], p->dtype);
+  int32_t page = p->b_page_table[page_entry(p, s, layer, j, p->d_out, n)];
+  return orc_decode(p->pages[(size_t)page * (size_t)p->page_elems + (size_t)(n % p->page_elems)], p->dtype);
 }
 
 /* Status bits for using slot s (s >= 0 assumed checked against num_slots by the caller).
@@ -186,12 +200,16 @@ static int32_t check_adapter(const orc_pool *p, int s, int layer, int need_a, in
   if (p->kind == ORC_POOL_PAGED) {
     for (int j = 0; j < r; ++j) {
       if (need_a) {
-        int32_t pa = p->a_page_table[table_index(p, s, layer, j)];
-        if (pa < 0 || pa >= p->num_pages) return ORC_BAD_PAGE;
+        for (int k = 0; k < p->d_in; k += p->page_elems) {
+          int32_t pa = p->a_page_table[page_entry(p, s, layer, j, p->d_in, k)];
+          if (pa < 0 || pa >= p->num_pages) return ORC_BAD_PAGE;
+        }
       }
       if (need_b) {
-        int32_t pb = p->b_page_table[table_index(p, s, layer, j)];
-        if (pb < 0 || pb >= p->num_pages) return ORC_BAD_PAGE;
+        for (int n = 0; n < p->d_out; n += p->page_elems) {
+          int32_t pb = p->b_page_table[page_entry(p, s, layer, j, p->d_out, n)];
+          if (pb < 0 || pb >= p->num_pages) return ORC_BAD_PAGE;
+        }
       }
     }
   }
@@ -208,7 +226,7 @@ static int check_pool(const orc_pool *p, int layer) {
     if (!p->a_t || !p->b) return ORC_ERR_ARG;
   } else if (p->kind == ORC_POOL_PAGED) {
     if (!p->pages || !p->a_page_table || !p->b_page_table) return ORC_ERR_ARG;
-    if (p->page_elems < p->d_in || p->page_elems < p->d_out || p->num_pages < 1) return ORC_ERR_ARG;
+    if (p->page_elems < 1 || p->num_pages < 1) return ORC_ERR_ARG;
   } else {
     return ORC_ERR_ARG;
   }

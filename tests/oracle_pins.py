@@ -81,27 +81,29 @@ def stacked(dtype, a_t_vals, b_vals, rank, scale):
 
 def to_paged(pool: O.Pool, rng, page_elems=None, extra_free=7):
     """Same adapters as a stacked pool, moved to randomly placed pages; free pages and page
-    tails hold NaN."""
+    tails hold NaN. A vector longer than page_elems is cut into ceil(d / page_elems) pages, each
+    placed at its own random position (S-LoRA "Unified Paging": a page is one H-vector)."""
     S, L, R = pool.num_slots, pool.num_layers, pool.r_max
     page_elems = max(pool.d_in, pool.d_out) + 3 if page_elems is None else page_elems
-    used = 2 * L * int(pool.rank.sum())
+    pa_n, pb_n = -(-pool.d_in // page_elems), -(-pool.d_out // page_elems)
+    used = L * int(pool.rank.sum()) * (pa_n + pb_n)
     num_pages = used + extra_free
-    phys = rng.permutation(num_pages)
+    phys = iter(rng.permutation(num_pages))
     nan = 0x7E01 if pool.dtype == FP16 else 0x7FC1
     pages = np.full((num_pages, page_elems), nan, np.uint16)
-    a_tab = np.full((S, L, R), -1, np.int32)
-    b_tab = np.full((S, L, R), -1, np.int32)
+    a_tab = np.full((S, L, R, pa_n), -1, np.int32)
+    b_tab = np.full((S, L, R, pb_n), -1, np.int32)
     a_t = pool.a_t.reshape(S, L, R, pool.d_in)
     b = pool.b.reshape(S, L, R, pool.d_out)
-    q = 0
     for s in range(S):
         for layer in range(L):
             for j in range(int(pool.rank[s])):
-                pa, pb = phys[q], phys[q + 1]
-                q += 2
-                a_tab[s, layer, j], b_tab[s, layer, j] = pa, pb
-                pages[pa, :pool.d_in] = a_t[s, layer, j]
-                pages[pb, :pool.d_out] = b[s, layer, j]
+                for tab, src, d, n in ((a_tab, a_t, pool.d_in, pa_n), (b_tab, b, pool.d_out, pb_n)):
+                    for q in range(n):
+                        pg = next(phys)
+                        tab[s, layer, j, q] = pg
+                        piece = src[s, layer, j, q * page_elems:(q + 1) * page_elems]
+                        pages[pg, :piece.size] = piece
     return O.Pool(dtype=pool.dtype, num_slots=S, num_layers=L, r_max=R, d_in=pool.d_in, d_out=pool.d_out,
                   rank=pool.rank, scale=pool.scale, pages=pages, a_page_table=a_tab, b_page_table=b_tab)
 
@@ -434,6 +436,33 @@ def pin_sgmv_equals_bgmv_on_the_same_rows(orc, seed=27):
                 assert np.array_equal(vs, vb, equal_nan=True), "v differs between the forms"
 
 
+def pin_vectors_across_pages_equal_stacked(orc, seed=28):
+    """S-LoRA "Unified Paging" with pages shorter than a vector (a rank-row of A^T or B spans
+    ceil(d / page_elems) pages, each at its own place in the pool): the same adapters give the
+    same bits as the stacked pool, for SGMV over random segments and for BGMV, in both dtypes, with
+    page sizes that divide d, that do not, and that exceed it."""
+    rng = np.random.default_rng(seed)
+    for dt in (BF16, FP16):
+        S, L, R, d_in, d_out, M = 4, 2, 6, 40, 24, 17
+        pool, _, _ = random_pool(rng, dt, S, L, R, d_in, d_out, ranks=rng.integers(1, R + 1, S))
+        cuts = np.sort(rng.integers(0, M + 1, 5))
+        off = np.r_[0, cuts, M].astype(np.int32)
+        ss = rng.integers(-1, S, len(off) - 1).astype(np.int32)
+        row_slot = rng.integers(-1, S, M).astype(np.int32)
+        x, y = random_act(rng, dt, M, d_in), random_act(rng, dt, M, d_out)
+        for pe in (8, 12, 24, 64):
+            paged = to_paged(pool, rng, page_elems=pe)
+            for layer in range(L):
+                want = orc.sgmv(pool, layer, x, y, off, ss)
+                got = orc.sgmv(paged, layer, x, y, off, ss)
+                assert got[3] == 0 and np.array_equal(got[0], want[0]), f"SGMV y differs with {pe}-element pages"
+                assert np.array_equal(got[1], want[1], equal_nan=True), f"SGMV v differs with {pe}-element pages"
+                want = orc.bgmv(pool, layer, x, y, row_slot)
+                got = orc.bgmv(paged, layer, x, y, row_slot)
+                assert got[3] == 0 and np.array_equal(got[0], want[0]), f"BGMV y differs with {pe}-element pages"
+
+
 ALL_PINS = [pin_decode_exhaustive, pin_round_trip_exhaustive, pin_round_matches_library, pin_round_ties,
             pin_identical_is_dense_gemm, pin_merged_identity, pin_rank_closed_form, pin_slot_identification,
-            pin_skip_rows_untouched, pin_status_contract, pin_sampled_rows, pin_sgmv_equals_bgmv_on_the_same_rows]
+            pin_skip_rows_untouched, pin_status_contract, pin_sampled_rows, pin_sgmv_equals_bgmv_on_the_same_rows,
+            pin_vectors_across_pages_equal_stacked]

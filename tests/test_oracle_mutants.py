@@ -41,6 +41,10 @@ MUTANTS = {
                               "int32_t s = off ? sgmv_row_slot(off, seg_slot, nseg, i) : row_slot[i + 1 < M ? i + 1 : i];"),
     "shrink_drops_top_rank_row": ("int r = p->rank[s];\n  for (int j = 0; j < r; ++j) {\n    double acc = 0.0;",
                                   "int r = p->rank[s] - 1;\n  for (int j = 0; j < r; ++j) {\n    double acc = 0.0;"),
+    "page_of_vector_start_only": ("  return table_index(p, s, layer, j) * (size_t)pages_per_vector(p, d) + (size_t)(k / p->page_elems);",
+                                  "  return table_index(p, s, layer, j) * (size_t)pages_per_vector(p, d) + (size_t)(k / p->page_elems) * 0;"),
+    "page_entry_of_next_vector_piece": ("  return table_index(p, s, layer, j) * (size_t)pages_per_vector(p, d) + (size_t)(k / p->page_elems);",
+                                        "  return table_index(p, s, layer, j) * (size_t)pages_per_vector(p, d) + (size_t)((k / p->page_elems + 1) % pages_per_vector(p, d));"),
     "x_element_shifted": ("acc += orc_decode(x_row[k], p->dtype) * elem_a(p, s, layer, k, j);",
                           "acc += orc_decode(x_row[k > 0 ? k - 1 : 0], p->dtype) * elem_a(p, s, layer, k, j);"),
 }
@@ -48,7 +52,7 @@ MUTANTS = {
 # the operator pins run first: they are cheap and catch most mutants
 ORDER = [P.pin_rank_closed_form, P.pin_slot_identification, P.pin_identical_is_dense_gemm, P.pin_merged_identity,
          P.pin_skip_rows_untouched, P.pin_status_contract, P.pin_sampled_rows, P.pin_sgmv_equals_bgmv_on_the_same_rows,
-         P.pin_round_ties,
+         P.pin_vectors_across_pages_equal_stacked, P.pin_round_ties,
          P.pin_round_trip_exhaustive, P.pin_decode_exhaustive, P.pin_round_matches_library]
 
 
