@@ -28,7 +28,7 @@ MLORA_MAX_RANK = 128
 STATUS_BAD_OFFSETS, STATUS_BAD_SLOT, STATUS_BAD_RANK, STATUS_BAD_PAGE, STATUS_TIMEOUT = 1, 2, 4, 8, 16
 ERR_NULL, ERR_DTYPE, ERR_SHAPE, ERR_ALIGN, ERR_POOL, ERR_CUDA, ERR_TOO_LARGE = -1, -2, -3, -4, -5, -6, -7
 NOALLOC_MAX_FLOATS = 1 << 20
-LAUNCH_PROGRAMMATIC = 1
+LAUNCH_PROGRAMMATIC, LAUNCH_GROUP_ROWS, LAUNCH_NO_GROUPING = 1, 2, 4
 
 _DT = {torch.bfloat16: MLORA_BF16, torch.float16: MLORA_FP16}
 
@@ -71,6 +71,7 @@ SIGNATURES = {
     "lora_bgmv_expand": [_V, _I64, _V, _PP, _V, _I32, _I32, _V, _V],
     "lora_sgmv": [_V, _I64, _V, _I64, _PP, _V, _V, _I32, _I32, _I32, _V, _V, _V],
     "lora_bgmv": [_V, _I64, _V, _I64, _PP, _V, _I32, _I32, _V, _V, _V],
+    "lora_bgmv_ex": [_V, _I64, _V, _I64, _PP, _V, _I32, _I32, _V, ctypes.c_uint32, _V, _V],
     "lora_sgmv_noalloc": [_V, _I64, _V, _I64, _PP, _V, _V, _I32, _I32, _I32, _V, _V],
     "lora_sgmv_grouped": [ctypes.POINTER(mlora_problem), _I32, _V, _V, _I32, _I32, _V, _V],
     "lora_sgmv_grouped_ex": [ctypes.POINTER(mlora_problem), _I32, _V, _V, _I32, _I32, ctypes.c_uint32, _V, _V],
@@ -226,6 +227,15 @@ def lora_bgmv(y, x, pool, row_slot, layer, v_scratch, status=None, stream=None):
     _check(lib().lora_bgmv(_dev(y, "y", h.dtype), _rows(y, "y", h.dtype), _dev(x, "x", h.dtype),
                            _rows(x, "x", h.dtype), h.ref, _i32(row_slot, "row_slot"), int(y.shape[0]), int(layer),
                            _dev(v_scratch, "v_scratch", torch.float32), _i32(status, "status"), _stream(stream)))
+
+
+def lora_bgmv_ex(y, x, pool, row_slot, layer, v_scratch, flags: int = 0, status=None, stream=None):
+    """lora_bgmv with launch flags (LAUNCH_GROUP_ROWS / LAUNCH_NO_GROUPING / LAUNCH_PROGRAMMATIC)."""
+    h = make_pool(pool)
+    _check(lib().lora_bgmv_ex(_dev(y, "y", h.dtype), _rows(y, "y", h.dtype), _dev(x, "x", h.dtype),
+                              _rows(x, "x", h.dtype), h.ref, _i32(row_slot, "row_slot"), int(y.shape[0]), int(layer),
+                              _dev(v_scratch, "v_scratch", torch.float32), int(flags), _i32(status, "status"),
+                              _stream(stream)))
 
 
 class Group:

@@ -19,6 +19,8 @@ namespace {
 
 thread_local char g_cuda_err[256] = "no CUDA error recorded";
 std::atomic<int64_t> g_launches{0};
+// lora_bgmv groups the rows of batches of at least this many rows on the device (bgmv_plan.cu).
+constexpr int32_t kGroupDefaultMinRows = 128;
 thread_local int g_pdl = 0;              // programmatic dependent launch for this thread's calls
 thread_local uint64_t g_wait_limit_ns = 0;  // testing hook: 0 = the kernels' default limit
 
@@ -44,8 +46,7 @@ int check_pool(const mlora_pool *p, int32_t layer, bool need_a, bool need_b) {
     if ((need_a && !aligned(p->a_t, 16)) || (need_b && !aligned(p->b, 16))) return MLORA_ERR_ALIGN;
   } else if (p->kind == MLORA_POOL_PAGED) {
     if (!p->pages || (need_a && !p->a_page_table) || (need_b && !p->b_page_table)) return MLORA_ERR_NULL;
-    if (p->num_pages < 1 || p->page_elems < (need_a ? p->d_in : 0) || p->page_elems < (need_b ? p->d_out : 0))
-      return MLORA_ERR_POOL;
+    if (p->num_pages < 1 || p->page_elems < 8 || p->page_elems > INT32_MAX) return MLORA_ERR_POOL;
     if (p->num_pages > INT32_MAX) return MLORA_ERR_POOL;  // page ids are int32
     if (!aligned(p->pages, 16) || p->page_elems % 8) return MLORA_ERR_ALIGN;
     if ((need_a && !aligned(p->a_page_table, 4)) || (need_b && !aligned(p->b_page_table, 4))) return MLORA_ERR_ALIGN;
@@ -73,6 +74,11 @@ mlora::PoolDev to_dev(const mlora_pool *p) {
   d.b_tab = p->b_page_table;
   d.rank = p->rank;
   d.scale = p->scale;
+  d.a_ppv = d.b_ppv = 1;
+  if (p->kind == MLORA_POOL_PAGED) {  // a vector longer than a page spans several
+    d.a_ppv = (int32_t)((p->d_in + p->page_elems - 1) / p->page_elems);
+    d.b_ppv = (int32_t)((p->d_out + p->page_elems - 1) / p->page_elems);
+  }
   return d;
 }
 
@@ -162,6 +168,14 @@ int run_tc(int mode, mlora::ProblemDev &q, const mlora_pool *pool, const int32_t
   tp.y = q.y;
   tp.ldy = q.ldy;
   tp.status = status;
+  tp.paged = q.pool.kind == MLORA_POOL_PAGED ? 1 : 0;
+  tp.page_elems = (int32_t)q.pool.page_elems;
+  tp.a_ppv = q.pool.a_ppv;
+  tp.b_ppv = q.pool.b_ppv;
+  tp.num_pages = q.pool.num_pages;
+  tp.pages = q.pool.pages;
+  tp.a_tab = q.pool.a_tab;
+  tp.b_tab = q.pool.b_tab;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (mode != mlora::MODE_EXPAND) {
     const cudaError_t e = mlora::launch_tc_shrink(q, tp, st);
@@ -317,18 +331,42 @@ int lora_sgmv_noalloc(void *y, int64_t ldy, const void *x, int64_t ldx, const ml
   return run_sgmv(mlora::MODE_FUSED, d, &pool, stream, g_pdl != 0);
 }
 
-int lora_bgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
-              int32_t num_rows, int32_t layer, float *v_scratch, int32_t *dev_status, void *stream) {
+int lora_bgmv_ex(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
+                 int32_t num_rows, int32_t layer, float *v_scratch, uint32_t flags, int32_t *dev_status,
+                 void *stream) {
+  if (flags & ~(MLORA_LAUNCH_PROGRAMMATIC | MLORA_LAUNCH_GROUP_ROWS | MLORA_LAUNCH_NO_GROUPING)) return MLORA_ERR_SHAPE;
   TRY(check_pool(pool, layer, true, true));
   TRY(check_v(v_scratch, num_rows));
   TRY(check_x(x, ldx, pool, num_rows));
   TRY(check_y(y, ldy, pool, num_rows));
   TRY(check_rows_bgmv(row_slot, num_rows, dev_status));
   if (num_rows == 0) return MLORA_OK;
+  const bool pdl = (flags & MLORA_LAUNCH_PROGRAMMATIC) != 0;
   mlora::DecodeParams d = base_params(nullptr, nullptr, 0, row_slot, num_rows, dev_status);
   d.prob[0] = problem(pool, layer, x, ldx, y, ldy, v_scratch);
   d.nprob = 1;
-  return run(mlora::MODE_FUSED, pool->dtype, d, stream, g_pdl != 0);
+  // Grouping: requested, or by default for batches large enough for repeated adapters to matter.
+  // The order goes to v_scratch (two int32 per row), which the fused kernel does not use.
+  const bool want = (flags & MLORA_LAUNCH_GROUP_ROWS) != 0 ||
+                    ((flags & MLORA_LAUNCH_NO_GROUPING) == 0 && num_rows >= kGroupDefaultMinRows);
+  if (want && num_rows <= mlora::kPlanMaxRows && pool->r_max >= 2) {
+    int32_t *perm = reinterpret_cast<int32_t *>(v_scratch);
+    int32_t *sslot = perm + num_rows;
+    const cudaError_t e = mlora::launch_bgmv_plan(row_slot, num_rows, d.prob[0].pool, perm, sslot,
+                                                  static_cast<cudaStream_t>(stream), pdl);
+    if (e != cudaSuccess) return cuda_fail(e, "row grouping launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    d.perm = perm;
+    d.sslot = sslot;
+    return run(mlora::MODE_FUSED, pool->dtype, d, stream, false);  // reads the order: no early start
+  }
+  return run(mlora::MODE_FUSED, pool->dtype, d, stream, pdl);
+}
+
+int lora_bgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
+              int32_t num_rows, int32_t layer, float *v_scratch, int32_t *dev_status, void *stream) {
+  return lora_bgmv_ex(y, ldy, x, ldx, pool, row_slot, num_rows, layer, v_scratch,
+                      g_pdl ? MLORA_LAUNCH_PROGRAMMATIC : 0u, dev_status, stream);
 }
 
 }  // extern "C"

@@ -61,16 +61,44 @@ struct TileInfo {
   int32_t pad;
 };
 
-__device__ __forceinline__ const uint16_t *a_row(const PoolDev &pl, int s, int layer, int j) {
-  const int64_t t = ((int64_t)s * pl.num_layers + layer) * pl.r_max + j;
-  if (pl.kind == MLORA_POOL_STACKED) return pl.a_t + t * pl.d_in;
-  return pl.pages + (int64_t)pl.a_tab[t] * pl.page_elems;
+// Element k of row j of A^T (d_in elements) or of B (d_out elements) of slot s, layer `layer`.
+// A paged vector spans ppv consecutive page-table entries: element k sits in entry
+// k / page_elems at offset k % page_elems (a chunk of 8 elements never straddles two pages:
+// page_elems is a multiple of 8). Square pages (ppv == 1) take one table entry per vector.
+__device__ __forceinline__ const uint16_t *paged_elem(const PoolDev &pl, const int32_t *tab, int ppv, int64_t t,
+                                                      int k) {
+  if (ppv == 1) return pl.pages + (int64_t)tab[t] * pl.page_elems + k;
+  const int pe = (int)pl.page_elems, q = k / pe;
+  return pl.pages + (int64_t)tab[t * ppv + q] * pl.page_elems + (k - q * pe);
 }
 
-__device__ __forceinline__ const uint16_t *b_row(const PoolDev &pl, int s, int layer, int j) {
+__device__ __forceinline__ const uint16_t *a_elem(const PoolDev &pl, int s, int layer, int j, int k) {
   const int64_t t = ((int64_t)s * pl.num_layers + layer) * pl.r_max + j;
-  if (pl.kind == MLORA_POOL_STACKED) return pl.b + t * pl.d_out;
-  return pl.pages + (int64_t)pl.b_tab[t] * pl.page_elems;
+  if (pl.kind == MLORA_POOL_STACKED) return pl.a_t + t * pl.d_in + k;
+  return paged_elem(pl, pl.a_tab, pl.a_ppv, t, k);
+}
+
+__device__ __forceinline__ const uint16_t *b_elem(const PoolDev &pl, int s, int layer, int j, int n) {
+  const int64_t t = ((int64_t)s * pl.num_layers + layer) * pl.r_max + j;
+  if (pl.kind == MLORA_POOL_STACKED) return pl.b + t * pl.d_out + n;
+  return paged_elem(pl, pl.b_tab, pl.b_ppv, t, n);
+}
+
+// f(ptr, off, count) for each piece of elements [k0, k1) of a vector that lies in one page (the
+// whole range for a stacked pool or square pages); off is the piece's first element minus k0.
+template <bool IS_A, class F>
+__device__ __forceinline__ void vec_pieces(const PoolDev &pl, int s, int layer, int j, int k0, int k1, F f) {
+  const int ppv = IS_A ? pl.a_ppv : pl.b_ppv;
+  if (pl.kind == MLORA_POOL_STACKED || ppv == 1) {
+    if (k1 > k0) f(IS_A ? a_elem(pl, s, layer, j, k0) : b_elem(pl, s, layer, j, k0), 0, k1 - k0);
+    return;
+  }
+  const int pe = (int)pl.page_elems;
+  for (int k = k0; k < k1;) {
+    const int end = min(k1, (k / pe + 1) * pe);
+    f(IS_A ? a_elem(pl, s, layer, j, k) : b_elem(pl, s, layer, j, k), k - k0, end - k);
+    k = end;
+  }
 }
 
 // Resolve virtual tile `t` of problem `pr` into `ti` (whole block participates; reads only
@@ -89,7 +117,7 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
   constexpr int SC = (SCAN_CAP + 1 + NTHREADS - 1) / NTHREADS;
   int32_t rk[RC], so[SC], ss[SC];
   float sc[RC];
-  int32_t row_slot = 0;
+  int32_t row_slot = 0, row_t = t;
 #pragma unroll
   for (int i = 0; i < RC; ++i) {
     const int q = tid + i * NTHREADS;
@@ -104,7 +132,14 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
     if (sgmv && q <= cnt0) so[i] = p.seg_off[q];
     if (sgmv && q < cnt0) ss[i] = p.seg_slot[q];
   }
-  if (!sgmv && tid == 0 && t < p.M) row_slot = p.row_slot[t];
+  if (!sgmv && tid == 0 && t < p.M) {
+    if (p.perm) {  // grouped order: tile t is row perm[t]
+      row_t = p.perm[t];
+      row_slot = p.sslot[t];
+    } else {
+      row_slot = p.row_slot[t];
+    }
+  }
 #pragma unroll
   for (int i = 0; i < RC; ++i) {
     const int q = tid + i * NTHREADS;
@@ -203,7 +238,7 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
     if (p.nseg == 0 && tid == 0 && scan[0] != p.M) ti->bad = MLORA_STATUS_BAD_OFFSETS;
     if (tid == 0) ti->skip = (found && !ti->bad) ? 0 : 1;
   } else if (tid == 0 && t < p.M) {
-    ti->row0 = t;
+    ti->row0 = row_t;
     ti->nr = 1;
     ti->slot = row_slot;
     ti->skip = 0;
@@ -229,16 +264,17 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
         } else if (pl.kind == MLORA_POOL_PAGED) {
           const int64_t t0 = ((int64_t)s * pl.num_layers + pr.layer) * pl.r_max;
           int32_t badp = 0;
-          for (int j = lane; j < rank; j += 32) {
-            if (MODE != MODE_EXPAND) {
-              const int32_t pg = pl.a_tab[t0 + j];
+          // every page of every vector j < rank this mode reads
+          if (MODE != MODE_EXPAND)
+            for (int e = lane; e < rank * pl.a_ppv; e += 32) {
+              const int32_t pg = pl.a_tab[t0 * pl.a_ppv + e];
               badp |= (pg < 0 || pg >= pl.num_pages);
             }
-            if (MODE != MODE_SHRINK) {
-              const int32_t pg = pl.b_tab[t0 + j];
+          if (MODE != MODE_SHRINK)
+            for (int e = lane; e < rank * pl.b_ppv; e += 32) {
+              const int32_t pg = pl.b_tab[t0 * pl.b_ppv + e];
               badp |= (pg < 0 || pg >= pl.num_pages);
             }
-          }
           if (__any_sync(0xffffffffu, badp)) bad = MLORA_STATUS_BAD_PAGE;
         }
       }
@@ -304,6 +340,29 @@ template <int JN>
 struct Rows {
   static constexpr int value = JN;
 };
+
+// Warp reduce-scatter of V partial sums (V a power of two, at most 32): every lane holds V
+// partials; afterwards each lane holds the warp's total of value (lane >> (5 - log2 V)), and the
+// 32 / V lanes of that group hold the same total. V - 1 + (5 - log2 V) shuffles instead of the
+// 5 V of a butterfly per value: at each halving step a lane keeps one half of its values and
+// receives its partner's sums of that half.
+template <int V>
+__device__ __forceinline__ float warp_reduce_scatter(float (&x)[V], int lane) {
+#pragma unroll
+  for (int cnt = V, s = 16; cnt > 1; cnt >>= 1, s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int k = 0; k < cnt / 2; ++k) {
+      const float give = upper ? x[k] : x[k + cnt / 2];
+      const float keep = upper ? x[k + cnt / 2] : x[k];
+      x[k] = keep + __shfl_xor_sync(0xffffffffu, give, s);
+    }
+  }
+  float t = x[0];
+#pragma unroll
+  for (int s = 16 / V; s > 0; s >>= 1) t += __shfl_xor_sync(0xffffffffu, t, s);
+  return t;
+}
 
 template <int DT, int MODE, int RT, int JPW>
 __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -415,24 +474,31 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
     }
     if (do_shrink && k_end - k_begin > kbn)
       for (int j = lane; j < rank; j += 32)
-        prefetch_l2(a_row(pl, s, pr.layer, j) + k_begin + kbn, (uint32_t)(k_end - k_begin - kbn) * 2);
+        vec_pieces<true>(pl, s, pr.layer, j, k_begin + kbn, k_end,
+                         [](const uint16_t *src, int, int n) { prefetch_l2(src, (uint32_t)n * 2); });
     if (clustered && lane == 0) mbar_arrive_expect_tx(xbar, (uint32_t)(cs * nr * rank * 4));
   }
   // A registers: in the Rows<JN> layout, register i = jj * (16 / JN) + u holds chunk
   // c8 = lane + 32 u of rank row j = warp + NWARPS jj (a[i / UK][i % UK]; JN = JPW is [jj][u]).
   uint4 a[JPW][UK];
+  const bool one_piece_a = pl.kind == MLORA_POOL_STACKED || pl.a_ppv == 1;
   auto load_a = [&](auto rows, int kb0) {
     constexpr int JN = decltype(rows)::value, UKN = 16 / JN;
     const int n8 = min(256 * UKN, k_end - kb0) >> 3;
 #pragma unroll
     for (int jj = 0; jj < JN; ++jj) {
       const int j = warp + jj * NWARPS;
+      // the vector's start when it lies in one page (stacked pool, square pages): one table read
+      // per rank row; else each chunk finds its page
+      const uint16_t *base = (j < rank && one_piece_a) ? a_elem(pl, s, pr.layer, j, 0) : nullptr;
 #pragma unroll
       for (int u = 0; u < UKN; ++u) {
         const int c8 = lane + 32 * u, i = jj * UKN + u;
+        const int k = kb0 + c8 * 8;
         // zero outside the slice and the rank: the one-row loop below then needs no guards
-        a[i / UK][i % UK] = (j < rank && c8 < n8) ? ldg_stream(a_row(pl, s, pr.layer, j) + kb0 + c8 * 8, evict_first)
-                                                  : make_uint4(0u, 0u, 0u, 0u);
+        a[i / UK][i % UK] = (j < rank && c8 < n8)
+                                ? ldg_stream(one_piece_a ? base + k : a_elem(pl, s, pr.layer, j, k), evict_first)
+                                : make_uint4(0u, 0u, 0u, 0u);
       }
     }
   };
@@ -442,13 +508,15 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
         if (lane == 0) mbar_arrive_expect_tx(bbar, (uint32_t)(rank * (n_end - n_begin) * 2));
         __syncwarp();
         for (int j = lane; j < rank; j += 32)
-          bulk_g2s_hint(bs + j * p.nb, b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2, bbar,
-                        evict_first);
+          vec_pieces<false>(pl, s, pr.layer, j, n_begin, n_end, [&](const uint16_t *src, int off, int n) {
+            bulk_g2s_hint(bs + j * p.nb + off, src, (uint32_t)n * 2, bbar, evict_first);
+          });
       } else if (!(x_bulk && RT == 1 && k_end - k_begin > kbn)) {
         // (a tile that loops over several passes of A prefetches its B rows at its last pass:
         // issued now, they would queue ahead of the later passes' A rows)
         for (int j = lane; j < rank; j += 32)
-          prefetch_l2(b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2);
+          vec_pieces<false>(pl, s, pr.layer, j, n_begin, n_end,
+                            [](const uint16_t *src, int, int n) { prefetch_l2(src, (uint32_t)n * 2); });
       }
   }
   if (x_bulk) {  // the bulk copies fill xs rows < nr up to the slice end; zeros elsewhere (disjoint bytes)
@@ -531,7 +599,8 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
           // prefetched them before the wait)
           if (pass > 0 && !b_staged && do_expand && n_end > n_begin && (pass + 1) * KBN >= k_end - k_begin)
             for (int j = tid; j < rank; j += NTHREADS)
-              prefetch_l2(b_row(pl, s, pr.layer, j) + n_begin, (uint32_t)(n_end - n_begin) * 2);
+              vec_pieces<false>(pl, s, pr.layer, j, n_begin, n_end,
+                                [](const uint16_t *src, int, int n) { prefetch_l2(src, (uint32_t)n * 2); });
 #pragma unroll
           for (int u = 0; u < UKN; ++u) {
             const uint4 xv = *reinterpret_cast<const uint4 *>(xp + (lane + 32 * u) * 8);
@@ -585,31 +654,36 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       }
     }
 
-    // warp-level sum of each (row, rank) dot product: every lane ends with the total
+    // Warp-level sums of the RT x JPW dot products (value q = i * JPW + jj): after the
+    // reduce-scatter, lane l holds the total of value l / LPV, in LPV replicas (lanes with the
+    // same value); V = RT * JPW partials, taken 32 at a time.
+    constexpr int V = RT * JPW;
+    constexpr int VG = V < 32 ? V : 32;  // values per reduce-scatter
+    constexpr int NG = V / VG;           // groups of 32 values (RT 4 x JPW 16: 2)
+    constexpr int LPV = 32 / VG;         // lanes per value
+    float tot[NG];
 #pragma unroll
-    for (int jj = 0; jj < JPW; ++jj) {
+    for (int g = 0; g < NG; ++g) {
+      float part[VG];
 #pragma unroll
-      for (int i = 0; i < RT; ++i) {
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) acc[i][jj] += __shfl_xor_sync(0xffffffffu, acc[i][jj], d);
-      }
+      for (int k = 0; k < VG; ++k) part[k] = acc[(g * VG + k) / JPW][(g * VG + k) % JPW];
+      tot[g] = warp_reduce_scatter<VG>(part, lane);
     }
+    const int myq = lane / LPV, rep = lane % LPV;  // this lane's value (within a group) and replica
 
     if (clustered) {
-      // Push this CTA's partials into slot c of every peer's gather buffer (lane q -> CTA q).
-      // A CTA that timed out pushes nothing; its peers then time out too and skip the tile.
+      // Push this CTA's partials into slot c of every peer's gather buffer: replica r of a value
+      // pushes it to peers r, r + LPV, ... A CTA that timed out pushes nothing; its peers then
+      // time out too and skip the tile.
       cluster_wait();  // every peer has initialised its exchange barrier
-      if (do_shrink && !timed_out && lane < cs) {
-        const uint32_t peer_gbuf = dsmem_addr(gbuf, lane);
-        const uint32_t peer_bar = dsmem_addr(xbar, lane);
+      if (do_shrink && !timed_out) {
 #pragma unroll
-        for (int jj = 0; jj < JPW; ++jj) {
+        for (int g = 0; g < NG; ++g) {
+          const int q = g * VG + myq, i = q / JPW, jj = q % JPW;
           const int j = warp + jj * NWARPS;
-          if (j < rank) {
-#pragma unroll
-            for (int i = 0; i < RT; ++i) {
-              if (i < nr) st_async_f32(peer_gbuf + 4u * (uint32_t)((c * RT + i) * p.r_alloc + j), acc[i][jj], peer_bar);
-            }
+          if (j < rank && i < nr) {
+            for (int peer = rep; peer < cs; peer += LPV)
+              st_async_f32(dsmem_addr(gbuf + (c * RT + i) * p.r_alloc + j, peer), tot[g], dsmem_addr(xbar, peer));
           }
         }
       }
@@ -631,18 +705,14 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       }
       // Every push into this CTA has landed (or the wait gave up, and the exit drains it): the
       // CTA needs nothing more from its peers and its shared memory is no longer written by them.
-    } else if (do_shrink && !timed_out && lane == 0) {
+    } else if (do_shrink && !timed_out && rep == 0) {
 #pragma unroll
-      for (int jj = 0; jj < JPW; ++jj) {
+      for (int g = 0; g < NG; ++g) {
+        const int q = g * VG + myq, i = q / JPW, jj = q % JPW;
         const int j = warp + jj * NWARPS;
-        if (j < rank) {
-#pragma unroll
-          for (int i = 0; i < RT; ++i) {
-            if (i < nr) {
-              if (MODE == MODE_SHRINK) pr.v[(int64_t)(row0 + i) * pl.r_max + j] = acc[i][jj];
-              else vsm[i * p.r_alloc + j] = acc[i][jj];
-            }
-          }
+        if (j < rank && i < nr) {
+          if (MODE == MODE_SHRINK) pr.v[(int64_t)(row0 + i) * pl.r_max + j] = tot[g];
+          else vsm[i * p.r_alloc + j] = tot[g];
         }
       }
     }
@@ -707,7 +777,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
               uint4 bq[UB];
               if (j0 + UB <= rank) {  // a whole batch of rank rows: no guards
 #pragma unroll
-                for (int u = 0; u < UB; ++u) bq[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+                for (int u = 0; u < UB; ++u) bq[u] = ldg_stream(b_elem(pl, s, pr.layer, j0 + u, n0), evict_first);
 #pragma unroll
                 for (int u = 0; u < UB; u += 2) {
                   add_row(bq[u], vr[j0 + u], ev);
@@ -716,7 +786,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
               } else if (j0 < rank) {
 #pragma unroll
                 for (int u = 0; u < UB; ++u)
-                  if (j0 + u < rank) bq[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+                  if (j0 + u < rank) bq[u] = ldg_stream(b_elem(pl, s, pr.layer, j0 + u, n0), evict_first);
 #pragma unroll
                 for (int u = 0; u < UB; u += 2) {
                   if (j0 + u < rank) add_row(bq[u], vr[j0 + u], ev);
@@ -737,7 +807,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
               uint4 bq[UB];
               if (j0 + UB <= rank) {  // a whole batch of rank rows: no guards
 #pragma unroll
-                for (int u = 0; u < UB; ++u) bq[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+                for (int u = 0; u < UB; ++u) bq[u] = ldg_stream(b_elem(pl, s, pr.layer, j0 + u, n0), evict_first);
 #pragma unroll
                 for (int u = 0; u < UB; u += 2) {
                   add_row(bq[u], vsm[j0 + u], ev);
@@ -746,7 +816,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
               } else {
 #pragma unroll
                 for (int u = 0; u < UB; ++u)
-                  if (j0 + u < rank) bq[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+                  if (j0 + u < rank) bq[u] = ldg_stream(b_elem(pl, s, pr.layer, j0 + u, n0), evict_first);
 #pragma unroll
                 for (int u = 0; u < UB; u += 2) {
                   if (j0 + u < rank) add_row(bq[u], vsm[j0 + u], ev);
@@ -800,7 +870,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
             uint4 b[UB];
 #pragma unroll
             for (int u = 0; u < UB; ++u)
-              if (j0 + u < rank) b[u] = ldg_stream(b_row(pl, s, pr.layer, j0 + u) + n0, evict_first);
+              if (j0 + u < rank) b[u] = ldg_stream(b_elem(pl, s, pr.layer, j0 + u, n0), evict_first);
 #pragma unroll
             for (int u = 0; u < UB; ++u)
               if (j0 + u < rank) add_row(b[u], j0 + u);

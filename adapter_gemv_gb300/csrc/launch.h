@@ -12,8 +12,9 @@ struct PoolDev {
   int32_t kind, dtype, num_slots, num_layers, r_max, d_in, d_out;
   const uint16_t *a_t, *b, *pages;
   int64_t page_elems, num_pages;
-  const int32_t *a_tab, *b_tab, *rank;
+  const int32_t *a_tab, *b_tab, *rank;  // paged: [slot][layer][r_max][a_ppv or b_ppv] page ids
   const float *scale;
+  int32_t a_ppv, b_ppv;  // paged: pages per vector, ceil(d_in / page_elems), ceil(d_out / page_elems)
 };
 
 enum { MODE_SHRINK = 0, MODE_EXPAND = 1, MODE_FUSED = 2 };
@@ -37,6 +38,7 @@ struct DecodeParams {
   const int32_t *seg_off, *seg_slot;  // SGMV (seg_off != nullptr)
   int32_t nseg;
   const int32_t *row_slot;  // BGMV
+  const int32_t *perm, *sslot;  // BGMV in grouped order (bgmv_plan.cu): tile t is row perm[t], slot sslot[t]
   int32_t M;
   int32_t *status;
   uint64_t wait_ns;  // limit of the kernel's waits (0 = the default, kWaitLimitNs)
@@ -59,6 +61,12 @@ struct TcParams {
   int32_t tc_min;  // segments of at least this many rows are this path's
   // chosen by the launcher
   int32_t rpad, ksplit, tiles, nper, nblk_total, tmem_cols, stages;
+  int32_t bm;  // rows per tile (a multiple of 8, at most the MMA's 128)
+  // paged pools: the A^T / B tiles are gathered row by row from the pages
+  int32_t paged, page_elems, a_ppv, b_ppv;
+  int64_t num_pages;
+  const uint16_t *pages;
+  const int32_t *a_tab, *b_tab;
 };
 
 constexpr int kTcMinRows = 32;
@@ -72,6 +80,12 @@ constexpr int kMaxDevices = 64;  // devices with a cached entry; others are quer
 bool tc_eligible(const PoolDev &pool, int num_rows, int nseg);
 cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stream);
 cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stream);
+
+// Device-side grouping of BGMV rows (bgmv_plan.cu): the rows in order of (rank descending, slot,
+// row) into perm / sslot [num_rows] each. At most kPlanMaxRows rows.
+constexpr int kPlanMaxRows = 4096;
+cudaError_t launch_bgmv_plan(const int32_t *row_slot, int32_t M, const PoolDev &pool, int32_t *perm, int32_t *sslot,
+                             cudaStream_t stream, bool pdl);
 
 // CUDA-core path for decode-sized tiles (decode_launch.cu chooses the split and the stages;
 // decode_{shrink,expand,fused}.cu hold the kernels). force_csplit > 0 overrides the split.

@@ -35,7 +35,8 @@ namespace mlora {
 
 namespace {
 
-constexpr int BM = 128;      // rows per tile (MMA M)
+constexpr int BM = 128;      // MMA M; a tile holds p.bm <= BM rows (the host's chunk size)
+constexpr int kMinTileRows = 64;  // smallest chunk the host picks
 constexpr int BK = 64;       // K elements per stage (one 128-byte swizzle row)
 constexpr int SKA = 2;  // shrink: swizzle atoms (64 K elements each) per ring stage: 256 contiguous
                         // bytes of each x row per stage (measured 2.5 % faster than one atom)
@@ -51,8 +52,8 @@ struct TcTile {
   float scale;
 };
 
-// Tile t = the t-th 128-row block, walking the segments in order: a segment of at least
-// p.tc_min rows contributes ceil(len / 128) blocks (the last one may be partial: nr < 128);
+// Tile t = the t-th block of p.bm rows, walking the segments in order: a segment of at least
+// p.tc_min rows contributes ceil(len / bm) blocks (the last one may be partial: nr < bm);
 // shorter segments belong to the CUDA-core kernels. Whole block participates; row metadata only.
 __device__ void resolve_tc_tile(const TcParams &p, int t, TcTile *ti, int32_t *scan) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -79,7 +80,7 @@ __device__ void resolve_tc_tile(const TcParams &p, int t, TcTile *ti, int32_t *s
           len = scan[q + 1] - lo;
           if (len < 0 || lo < 0 || scan[q + 1] > p.M) bad = 1;
         }
-        const int32_t nt = (q < cnt && len >= p.tc_min && len > 0) ? (len + BM - 1) / BM : 0;
+        const int32_t nt = (q < cnt && len >= p.tc_min && len > 0) ? (len + p.bm - 1) / p.bm : 0;
         int32_t incl = nt;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -89,8 +90,8 @@ __device__ void resolve_tc_tile(const TcParams &p, int t, TcTile *ti, int32_t *s
         const int32_t excl = carry + incl - nt;
         const bool mine = q < cnt && t >= excl && t < excl + nt;
         if (!found && mine) {
-          ti->row0 = lo + (t - excl) * BM;
-          ti->nr = min(BM, len - (t - excl) * BM);
+          ti->row0 = lo + (t - excl) * p.bm;
+          ti->nr = min(p.bm, len - (t - excl) * p.bm);
           ti->slot = scan[SCAN_CAP + 1 + q];
         }
         found |= __any_sync(0xffffffffu, mine);
@@ -127,6 +128,46 @@ __device__ void resolve_tc_tile(const TcParams &p, int t, TcTile *ti, int32_t *s
   __syncthreads();
 }
 
+// Paged pools: the page ids of the tile's vectors (rows j < rpad of A^T or of B, for the tile's slot
+// and layer), ptab[j * ppv + q] = page of the q-th piece of vector j, -1 for j >= rank (those rows
+// are zero-filled). Whole block; true if a page id lies outside the pool (BAD_PAGE).
+__device__ bool load_page_ids(const TcParams &p, const int32_t *tab, int ppv, int s, int rank, int32_t *ptab) {
+  const int64_t t0 = ((int64_t)s * p.num_layers + p.layer) * p.r_max;
+  int bad = 0;
+  for (int e = threadIdx.x; e < p.rpad * ppv; e += blockDim.x) {
+    int32_t pg = -1;
+    if (e / ppv < rank) {
+      pg = tab[t0 * ppv + e];
+      bad |= (pg < 0 || pg >= p.num_pages) ? 1 : 0;
+    }
+    ptab[e] = pg;
+  }
+  return __syncthreads_or(bad) != 0;
+}
+
+// Paged pools: one 64-element K-major (A^T) or MN-major (B) atom of rows j < rpad, elements
+// [e0, e0 + 64) of each vector (d elements long), copied by the calling warp with 16-byte cp.async
+// into the 128-byte-swizzled layout a TMA load would write (row j at j * 128, chunk cc at
+// (cc ^ (j % 8)) * 16). Chunks past the vector's end or of rows j >= rank are zero-filled. A
+// piece of 8 elements never straddles pages (page_elems is a multiple of 8, at least 64, so an
+// atom crosses at most one page boundary).
+__device__ __forceinline__ void gather_atom(const TcParams &p, const int32_t *ptab, int ppv, int d, int e0,
+                                            uint8_t *dst, int lane) {
+  const int pe = p.page_elems;
+  const int pq = e0 / pe, rq = e0 - pq * pe;
+  for (int e = lane; e < p.rpad * 8; e += 32) {
+    const int j = e >> 3, cc = e & 7;
+    int off = rq + cc * 8, pidx = pq;
+    if (off >= pe) {
+      off -= pe;
+      ++pidx;
+    }
+    const int32_t pg = (e0 + cc * 8 < d) ? ptab[j * ppv + pidx] : -1;
+    const uint16_t *src = pg >= 0 ? p.pages + (int64_t)pg * pe + off : p.pages;
+    tc::cp_async16(dst + j * 128 + ((cc ^ (j & 7)) << 4), src, pg >= 0 ? 16u : 0u);
+  }
+}
+
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
@@ -136,15 +177,22 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 
 struct ShrinkSmem {
   int stages, stage_bytes, a_off, bar_off, total;
+  // A stage holds the SKA swizzle atoms of the X tile (bm rows of 128 B each, atom q at
+  // q * bm * 128) and then those of the A^T rows (rpad rows each). The MMA reads 128 rows from
+  // an X atom: for bm < 128 the rows past bm are whatever follows in shared memory (their sums
+  // land in accumulator rows that are never stored); the pad after the ring keeps every such
+  // read inside the allocation.
   // stages = 0: as many as fit in 227 KB (a deep ring keeps one CTA's TMA loads streaming)
-  __host__ __device__ static ShrinkSmem make(int rpad, int stages = 0) {
+  __host__ __device__ static ShrinkSmem make(int rpad, int bm, int stages = 0) {
     ShrinkSmem L;
-    L.a_off = SKA * BM * BK * 2;                                     // X tile: SKA x 16 KB (atom q at q * 16 KB)
-    L.stage_bytes = (L.a_off + SKA * rpad * BK * 2 + 1023) & ~1023;  // + A^T rows
-    const int fixed = 1024 + (2 * SCAN_CAP + 1) * 4 + 1024;   // barriers, tile info, scan, alignment slack
-    if (stages <= 0) stages = (227 * 1024 - fixed) / L.stage_bytes;
+    L.a_off = SKA * bm * BK * 2;
+    L.stage_bytes = (L.a_off + SKA * rpad * BK * 2 + 1023) & ~1023;
+    const int overhang = (SKA - 1) * bm * 128 + BM * 128 - L.stage_bytes;  // last atom's 128-row read
+    const int pad = overhang > 0 ? (overhang + 1023) & ~1023 : 0;
+    const int fixed = 1024 + (2 * SCAN_CAP + 1) * 4 + 1024;  // barriers, tile info, scan, alignment slack
+    if (stages <= 0) stages = (227 * 1024 - fixed - pad) / L.stage_bytes;
     L.stages = stages < 2 ? 2 : stages > MAX_STAGES ? MAX_STAGES : stages;
-    L.bar_off = L.stages * L.stage_bytes;
+    L.bar_off = L.stages * L.stage_bytes + pad;
     L.total = L.bar_off + fixed;
     return L;
   }
@@ -156,7 +204,7 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
                                                              const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  const ShrinkSmem L = ShrinkSmem::make(p.rpad, p.stages);
+  const ShrinkSmem L = ShrinkSmem::make(p.rpad, p.bm, p.stages);
   const int STAGES = L.stages;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
   uint64_t *empty = full + MAX_STAGES;
@@ -174,7 +222,7 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], p.paged ? 1 + 32 : 1);  // paged: + one cp.async arrival per producer lane
       mbar_init(&empty[s], 1);
     }
     mbar_init(accbar, 1);
@@ -190,18 +238,50 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
   const uint32_t tmem = *tmem_slot;
 
   resolve_tc_tile(p, t, ti, scan);
-  if (c == 0 && tid == 0 && ti->bad) report(p.status, ti->bad);
-  const bool active = !ti->skip;
+  int32_t *ptab = scan;  // paged: the scan area is free after the resolve
+  bool active = !ti->skip;
+  int32_t bad = ti->bad;
+  if (p.paged && active && load_page_ids(p, p.a_tab, p.a_ppv, ti->slot, ti->rank, ptab)) {
+    bad |= MLORA_STATUS_BAD_PAGE;
+    active = false;
+  }
+  if (c == 0 && tid == 0 && bad) report(p.status, bad);
   const int row0 = ti->row0, nr = ti->nr, s = ti->slot, rank = ti->rank;
   const int kb_total = (p.d_in + SKA * BK - 1) / (SKA * BK);
   const int kb_per = (kb_total + ks - 1) / ks;
   const int kb0 = min((int)c * kb_per, kb_total), kb1 = min(kb0 + kb_per, kb_total);
   const int nkb = active ? kb1 - kb0 : 0;
   const int arow = (s * p.num_layers + p.layer) * p.r_max;
-  const uint32_t stage_tx = (uint32_t)(SKA * (BM * BK * 2 + p.rpad * BK * 2));
+  // bytes the stage's TMA loads bring: the X tile, and the A^T rows unless they are gathered
+  const uint32_t stage_tx = (uint32_t)(SKA * (p.bm * BK * 2 + (p.paged ? 0 : p.rpad * BK * 2)));
   const uint32_t idesc = tc::idesc_f16(DT == MLORA_BF16, false, false, BM, p.rpad);
 
-  if (warp == 0) {
+  if (warp == 0 && p.paged) {
+    // producer (whole warp): lane 0 TMA-loads the X tile of each K block, and the warp gathers the
+    // A^T rows from their pages with cp.async (completing on the same barrier)
+    for (int i = 0; i < nkb; ++i) {
+      const int st = i % STAGES;
+      const int ok = (i < STAGES || mbar_wait(&empty[st], (uint32_t)((i / STAGES) - 1) & 1u)) ? 1 : 0;
+      if (__any_sync(0xffffffffu, !ok)) {
+        if (lane == 0) flags[0] = 1;
+        break;
+      }
+      uint8_t *sb = smem + st * L.stage_bytes;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[st], stage_tx);
+        for (int q = 0; q < SKA; ++q)
+          tc::tma_load_2d(sb + q * p.bm * 128, &tm_x, ((kb0 + i) * SKA + q) * BK, row0, &full[st]);
+      }
+      for (int q = 0; q < SKA; ++q)
+        gather_atom(p, ptab, p.a_ppv, p.d_in, ((kb0 + i) * SKA + q) * BK, sb + L.a_off + q * p.rpad * 128, lane);
+      tc::cp_async_arrive(&full[st]);
+    }
+    // nothing may land in shared memory after the CTA exits: the last stages' copies (bounded)
+    if (lane == 0)
+      for (int i = max(nkb - STAGES, 0); i < nkb; ++i)
+        (void)mbar_wait(&full[i % STAGES], (uint32_t)(i / STAGES) & 1u, kDrainLimitNs);
+    __syncwarp();
+  } else if (warp == 0) {
     // producer (one lane): TMA X tile and A^T rows of each K block into the ring
     for (int i = 0; lane == 0 && i < nkb; ++i) {
       const int st = i % STAGES;
@@ -212,7 +292,7 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
       uint8_t *sb = smem + st * L.stage_bytes;
       mbar_arrive_expect_tx(&full[st], stage_tx);
       for (int q = 0; q < SKA; ++q) {
-        tc::tma_load_2d(sb + q * BM * 128, &tm_x, ((kb0 + i) * SKA + q) * BK, row0, &full[st]);
+        tc::tma_load_2d(sb + q * p.bm * 128, &tm_x, ((kb0 + i) * SKA + q) * BK, row0, &full[st]);
         tc::tma_load_2d(sb + L.a_off + q * p.rpad * 128, &tm_a, ((kb0 + i) * SKA + q) * BK, arow, &full[st]);
       }
     }
@@ -225,12 +305,13 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
         flags[0] = 1;
         break;
       }
+      if (p.paged) tc::fence_proxy_async();  // the cp.async-gathered A^T rows -> the tensor cores
       tc::tc_fence_after();
       const uint8_t *sb = smem + st * L.stage_bytes;
 #pragma unroll
       for (int k = 0; k < SKA * BK / 16; ++k) {
         const int q = k / (BK / 16), kk = k % (BK / 16);
-        const uint64_t da = tc::smem_desc_sw128(sb + q * BM * 128 + kk * 32, 16, 1024);
+        const uint64_t da = tc::smem_desc_sw128(sb + q * p.bm * 128 + kk * 32, 16, 1024);
         const uint64_t db = tc::smem_desc_sw128(sb + L.a_off + q * p.rpad * 128 + kk * 32, 16, 1024);
         tc::mma_f16(tmem, da, db, idesc, (i > 0 || k > 0) ? 1u : 0u);
       }
@@ -275,7 +356,7 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
     cluster_sync();
     if (active && !timed_out) {
       // CTA c sums rows [c * rp, min(128, (c + 1) * rp)) over the cluster, in rank order
-      const int rp = (BM + ks - 1) / ks;
+      const int rp = (p.bm + ks - 1) / ks;
       const int m_lo = min((int)c * rp, nr), m_hi = min(m_lo + rp, nr);
       for (int e = tid; e < (m_hi - m_lo) * rank; e += NTHREADS) {
         const int mm = m_lo + e / rank, j = e % rank;
@@ -304,17 +385,18 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
 constexpr int EXP_EPI_WARPS = 8;
 constexpr int EXP_THREADS = (EXP_EPI_WARPS + 3) * 32;
 
-// Shared memory: V hi / lo, then EBUF pipeline buffers, each with the y tile of one 64-column
-// block (128 rows x 128 B) followed by its B rows (one MN atom: rpad K rows x 128 B).
+// Shared memory: V hi / lo (128 rows: the MMA's M), then EBUF pipeline buffers, each with the y
+// tile of one 64-column block (bm rows x 128 B) followed by its B rows (one MN atom: rpad K rows
+// x 128 B).
 struct ExpandSmem {
   int nbuf, v_off, buf_off, buf_bytes, b_in_buf, bar_off, total;
   // nbuf = 0: as many buffers as fit in `budget` bytes
-  __host__ __device__ static ExpandSmem make(int rpad, int nbuf = 0, int budget = 227 * 1024) {
+  __host__ __device__ static ExpandSmem make(int rpad, int bm, int nbuf = 0, int budget = 227 * 1024) {
     ExpandSmem L;
     const int katoms = (rpad + BK - 1) / BK;
     L.v_off = 0;
     L.buf_off = 2 * katoms * BM * 128;
-    L.b_in_buf = BM * 128;
+    L.b_in_buf = bm * 128;
     L.buf_bytes = (L.b_in_buf + rpad * 128 + 1023) & ~1023;
     const int fixed = 1024 + (2 * SCAN_CAP + 1) * 4 + 1024;
     if (nbuf <= 0) nbuf = (budget - fixed - L.buf_off) / L.buf_bytes;
@@ -333,7 +415,7 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
                                                                 const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  const ExpandSmem L = ExpandSmem::make(p.rpad, p.stages);
+  const ExpandSmem L = ExpandSmem::make(p.rpad, p.bm, p.stages);
   const int EBUF = L.nbuf;
   const int katoms = (p.rpad + BK - 1) / BK;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);  // [EBUF] y tile + B rows landed
@@ -355,7 +437,7 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
 
   if (tid == 0) {
     for (int b = 0; b < EBUF; ++b) {
-      mbar_init(&full[b], 1);
+      mbar_init(&full[b], p.paged ? 1 + 32 : 1);  // paged: + one cp.async arrival per producer lane
       mbar_init(&empty[b], 1);
       mbar_init(&ystaged[b], EXP_EPI_WARPS * 32);
     }
@@ -376,27 +458,42 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
   const uint32_t tmem = *tmem_slot;
 
   resolve_tc_tile(p, t, ti, scan);  // every thread; ends with a barrier
-  if (blockIdx.x == 0 && tid == 0 && ti->bad) report(p.status, ti->bad);
-  const bool active = !ti->skip && nblk > 0;
+  int32_t *ptab = scan;               // paged: the scan area is free after the resolve
+  bool active = !ti->skip && nblk > 0;
+  int32_t bad = ti->bad;
+  if (p.paged && active && load_page_ids(p, p.b_tab, p.b_ppv, ti->slot, ti->rank, ptab)) {
+    bad |= MLORA_STATUS_BAD_PAGE;
+    active = false;
+  }
+  if (blockIdx.x == 0 && tid == 0 && bad) report(p.status, bad);
   const int row0 = ti->row0, nr = ti->nr, s = ti->slot, rank = ti->rank;
   const float scale = ti->scale;
-  const bool full_tile = nr == BM;  // a partial tile writes its rows with plain stores: the
+  const bool full_tile = nr == p.bm;  // a partial tile writes its rows with plain stores: the
                                     // rows past nr belong to another segment
   const int brow = (s * p.num_layers + p.layer) * p.r_max;
-  const uint32_t block_tx = (uint32_t)(p.rpad * 128 + BM * 128);
+  // bytes a block's TMA loads bring: the y tile, and the B rows unless they are gathered
+  const uint32_t block_tx = (uint32_t)((p.paged ? 0 : p.rpad * 128) + p.bm * 128);
   const uint32_t idesc = tc::idesc_f16(DT == MLORA_BF16, false, true, BM, EBN);
   auto buf = [&](int i) { return smem + L.buf_off + (i % EBUF) * L.buf_bytes; };
 
   // producer: the first EBUF blocks go out before V is built
   int issued = 0;
+  // one block's loads: lane 0 TMA-loads the y tile (and B rows of a stacked pool); for a paged
+  // pool the whole producer warp gathers the B rows from their pages with cp.async
   auto issue = [&](int i) {
     uint8_t *dst = buf(i);
     const int nb = nb_begin + i;
-    mbar_arrive_expect_tx(&full[i % EBUF], block_tx);
-    tc::tma_load_2d(dst, &tm_y, nb * EBN, row0, &full[i % EBUF]);
-    tc::tma_load_2d(dst + BM * 128, &tm_b, nb * EBN, brow, &full[i % EBUF]);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&full[i % EBUF], block_tx);
+      tc::tma_load_2d(dst, &tm_y, nb * EBN, row0, &full[i % EBUF]);
+      if (!p.paged) tc::tma_load_2d(dst + L.b_in_buf, &tm_b, nb * EBN, brow, &full[i % EBUF]);
+    }
+    if (p.paged) {
+      gather_atom(p, ptab, p.b_ppv, p.d_out, nb * EBN, dst + L.b_in_buf, lane);
+      tc::cp_async_arrive(&full[i % EBUF]);
+    }
   };
-  if (active && warp == EXP_EPI_WARPS && lane == 0)
+  if (active && warp == EXP_EPI_WARPS && (p.paged || lane == 0))
     for (; issued < nblk && issued < EBUF; ++issued) issue(issued);
 
   // V hi / lo in the K-major 128-byte-swizzle layout: epilogue thread m owns row m. fp16 rows
@@ -464,19 +561,22 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
   __syncthreads();
 
   if (active && warp == EXP_EPI_WARPS) {
-    // ---- producer (one lane): refill a buffer once its y tile has been stored
-    if (lane == 0) {
+    // ---- producer (lane 0, or the whole warp for a paged pool): refill a buffer once its y
+    // tile has been stored
+    if (p.paged || lane == 0) {
       for (; issued < nblk; ++issued) {
         const int i = issued;
-        if (!mbar_wait(&empty[i % EBUF], (uint32_t)((i / EBUF) - 1) & 1u)) {
-          flags[0] = 1;
+        const int ok = mbar_wait(&empty[i % EBUF], (uint32_t)((i / EBUF) - 1) & 1u) ? 1 : 0;
+        if (p.paged ? __any_sync(0xffffffffu, !ok) : !ok) {
+          if (lane == 0) flags[0] = 1;
           break;
         }
         issue(i);
       }
       // nothing may land in shared memory after the CTA exits: wait for the last loads (bounded)
-      for (int i = max(issued - EBUF, 0); i < issued; ++i)
-        (void)mbar_wait(&full[i % EBUF], (uint32_t)(i / EBUF) & 1u, kDrainLimitNs);
+      if (lane == 0)
+        for (int i = max(issued - EBUF, 0); i < issued; ++i)
+          (void)mbar_wait(&full[i % EBUF], (uint32_t)(i / EBUF) & 1u, kDrainLimitNs);
     }
     __syncwarp();
   } else if (active && warp == EXP_EPI_WARPS + 1) {
@@ -490,7 +590,8 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
           flags[0] = 1;
           break;
         }
-        uint8_t *bs = buf(i) + BM * 128;
+        uint8_t *bs = buf(i) + L.b_in_buf;
+        if (p.paged) tc::fence_proxy_async();  // the cp.async-gathered B rows -> the tensor cores
         if (rank < p.rpad) {  // rows rank..rpad-1 of B are padding (possibly NaN): zero them
           for (int e = 0; e < (p.rpad - rank) * 8; ++e)
             *reinterpret_cast<uint4 *>(bs + (rank + e / 8) * 128 + (e % 8) * 16) = make_uint4(0, 0, 0, 0);
@@ -559,18 +660,20 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
       }
       tc::tc_fence_before();
       mbar_arrive(&accempty[a]);  // the accumulator may take the block after next
+      if (m < nr) {  // accumulator rows past the tile's rows (m >= nr, at most bm) are not the tile's
 #pragma unroll
-      for (int cq = 0; cq < EBN / 16; ++cq) {  // this warp's 16-byte chunks of the 128-byte row
-        const int ch = half * (EBN / 16) + cq;
-        uint4 *cell = reinterpret_cast<uint4 *>(ys + m * 128 + ((ch ^ (m & 7)) << 4));
-        float yf[8];
-        unpack8<DT>(*cell, yf);
+        for (int cq = 0; cq < EBN / 16; ++cq) {  // this warp's 16-byte chunks of the 128-byte row
+          const int ch = half * (EBN / 16) + cq;
+          uint4 *cell = reinterpret_cast<uint4 *>(ys + m * 128 + ((ch ^ (m & 7)) << 4));
+          float yf[8];
+          unpack8<DT>(*cell, yf);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) yf[e] = fmaf(rscale, d[cq * 8 + e], yf[e]);
-        if (full_tile) {
-          *cell = pack8<DT>(yf);
-        } else if (m < nr && nb * EBN + ch * 8 < p.d_out) {
-          *reinterpret_cast<uint4 *>(p.y + (int64_t)(row0 + m) * p.ldy + nb * EBN + ch * 8) = pack8<DT>(yf);
+          for (int e = 0; e < 8; ++e) yf[e] = fmaf(rscale, d[cq * 8 + e], yf[e]);
+          if (full_tile) {
+            *cell = pack8<DT>(yf);
+          } else if (nb * EBN + ch * 8 < p.d_out) {
+            *reinterpret_cast<uint4 *>(p.y + (int64_t)(row0 + m) * p.ldy + nb * EBN + ch * 8) = pack8<DT>(yf);
+          }
         }
       }
       tc::fence_proxy_async();          // this thread's y writes -> visible to the TMA store
@@ -636,9 +739,24 @@ constexpr int TC_MIN_ROWS = kTcMinRows;
 // with decode rows). They take every segment of at least kTcMinRows rows; the CUDA-core kernel
 // takes the rest. A decode batch (a few rows per segment) runs on the CUDA-core kernel alone.
 bool tc_eligible(const PoolDev &pool, int num_rows, int nseg) {
-  return pool.kind == MLORA_POOL_STACKED && (pool.dtype == MLORA_BF16 || pool.dtype == MLORA_FP16) &&
+  const int rpad = (pool.r_max + 15) & ~15;
+  // paged pools: pages of at least 64 elements (an atom crosses at most one page boundary), and
+  // the page ids of a tile's vectors fit the table area of shared memory
+  const bool paged_ok = pool.kind == MLORA_POOL_PAGED && pool.page_elems >= 64 &&
+                        rpad * pool.a_ppv <= 2 * SCAN_CAP && rpad * pool.b_ppv <= 2 * SCAN_CAP;
+  return (pool.kind == MLORA_POOL_STACKED || paged_ok) && (pool.dtype == MLORA_BF16 || pool.dtype == MLORA_FP16) &&
          pool.r_max <= 128 && num_rows >= kTcBatchRows &&
          (int64_t)num_rows >= (int64_t)kTcAvgRows * (nseg > 0 ? nseg : 1) && encoder() != nullptr;
+}
+
+// Rows per tile: chunks small enough that the tiles of the long segments fill the SMs in one wave
+// (at most M / bm + nseg tiles), a multiple of 8 rows (the swizzle atom), between kMinTileRows
+// and the MMA's 128.
+int tile_rows(int M, int nseg) {
+  const int avail = sm_count() - nseg;
+  int bm = BM;
+  if (avail > 0) bm = ((M + avail - 1) / avail + 7) & ~7;
+  return bm < kMinTileRows ? kMinTileRows : bm > BM ? BM : bm;
 }
 
 cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stream) {
@@ -646,11 +764,12 @@ cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stre
   p.rpad = (pl.r_max + 15) & ~15;
   p.tmem_cols = p.rpad <= 32 ? 32 : p.rpad <= 64 ? 64 : 128;
   p.tc_min = TC_MIN_ROWS;
-  p.tiles = p.M / BM + p.nseg;  // >= sum over long segments of ceil(len / 128)
+  p.bm = tile_rows(p.M, p.nseg);
+  p.tiles = p.M / p.bm + p.nseg;  // >= sum over long segments of ceil(len / bm)
   if (p.tiles <= 0) return cudaSuccess;
   const int kb_total = (pl.d_in + SKA * BK - 1) / (SKA * BK);
-  p.stages = ShrinkSmem::make(p.rpad).stages;
-  const size_t smem = ShrinkSmem::make(p.rpad, p.stages).total;
+  p.stages = ShrinkSmem::make(p.rpad, p.bm).stages;
+  const size_t smem = ShrinkSmem::make(p.rpad, p.bm, p.stages).total;
   auto kern = pl.dtype == MLORA_BF16 ? tc_shrink_kernel<MLORA_BF16> : tc_shrink_kernel<MLORA_FP16>;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
@@ -662,9 +781,13 @@ cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stre
   ks = ks > kb_total ? kb_total : ks;
   p.ksplit = ks;
   CUtensorMap tm_x, tm_a;
-  if (!encode_2d(&tm_x, pl.dtype, pr.x, pl.d_in, p.M, pr.ldx, BM)) return cudaErrorInvalidValue;
-  if (!encode_2d(&tm_a, pl.dtype, pl.a_t, pl.d_in, (int64_t)pl.num_slots * pl.num_layers * pl.r_max, pl.d_in, p.rpad))
+  if (!encode_2d(&tm_x, pl.dtype, pr.x, pl.d_in, p.M, pr.ldx, p.bm)) return cudaErrorInvalidValue;
+  if (p.paged) {
+    tm_a = tm_x;  // not read: the A^T rows are gathered from the pages
+  } else if (!encode_2d(&tm_a, pl.dtype, pl.a_t, pl.d_in, (int64_t)pl.num_slots * pl.num_layers * pl.r_max, pl.d_in,
+                        p.rpad)) {
     return cudaErrorInvalidValue;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ks, p.tiles, 1);
   cfg.blockDim = dim3(NTHREADS, 1, 1);
@@ -684,7 +807,10 @@ cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stre
   const PoolDev &pl = pr.pool;
   p.rpad = (pl.r_max + 15) & ~15;
   p.tc_min = TC_MIN_ROWS;
-  p.tiles = p.M / BM + p.nseg;
+  // Full 128-row tiles: the expand's cost per block is its y tile's pipeline pass, and tiles of
+  // fewer rows measured slower (13B prefill, 7 expands: 689 us with 128 rows, 776 us with 88).
+  p.bm = BM;
+  p.tiles = p.M / p.bm + p.nseg;
   if (p.tiles <= 0) return cudaSuccess;
   p.nblk_total = (pl.d_out + EBN - 1) / EBN;
   // Column runs per tile: the grid is about two waves of the expand's two CTAs per SM (measured
@@ -697,11 +823,15 @@ cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stre
   }
   const int expand_budget = 112 * 1024;  // two CTAs per SM
   CUtensorMap tm_b, tm_y;
-  if (!encode_2d(&tm_b, pl.dtype, pl.b, pl.d_out, (int64_t)pl.num_slots * pl.num_layers * pl.r_max, pl.d_out, p.rpad))
+  if (!encode_2d(&tm_y, pl.dtype, pr.y, pl.d_out, p.M, pr.ldy, p.bm)) return cudaErrorInvalidValue;
+  if (p.paged) {
+    tm_b = tm_y;  // not read: the B rows are gathered from the pages
+  } else if (!encode_2d(&tm_b, pl.dtype, pl.b, pl.d_out, (int64_t)pl.num_slots * pl.num_layers * pl.r_max, pl.d_out,
+                        p.rpad)) {
     return cudaErrorInvalidValue;
-  if (!encode_2d(&tm_y, pl.dtype, pr.y, pl.d_out, p.M, pr.ldy, BM)) return cudaErrorInvalidValue;
-  p.stages = ExpandSmem::make(p.rpad, 0, expand_budget).nbuf;
-  const size_t smem = ExpandSmem::make(p.rpad, p.stages).total;
+  }
+  p.stages = ExpandSmem::make(p.rpad, p.bm, 0, expand_budget).nbuf;
+  const size_t smem = ExpandSmem::make(p.rpad, p.bm, p.stages).total;
   auto kern = pl.dtype == MLORA_BF16 ? tc_expand_kernel<MLORA_BF16> : tc_expand_kernel<MLORA_FP16>;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;

@@ -57,6 +57,22 @@ __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.b
 // Make generic-proxy writes to shared memory visible to the async proxy (TMA, tensor cores).
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// ---- 16-byte asynchronous copies (global -> shared), for tiles gathered row by row ----------
+
+// Copy 16 bytes (both addresses 16-byte aligned) into shared memory without registers; with
+// src_bytes == 0 nothing is read and the 16 bytes are zero-filled.
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src_gmem, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)), "l"(src_gmem),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued so far has landed (the arrival is
+// counted in the barrier's expected count: .noinc).
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // ---- TMEM --------------------------------------------------------------------------------------
 
 // Whole warp: allocate `ncols` (power of two >= 32) TMEM columns; the address lands in *dst.

@@ -31,11 +31,16 @@
  *            (Punica's LoraWeight, zh-TW digest section 5.4: wa [layers, r, in_features],
  *            wb [layers, r, out_features]; slots padded to the largest rank as in the
  *            reference loop). Rows j >= rank[s] are never read.
- *   paged    S-LoRA (arXiv 2311.03285) "Unified Paging": one page per rank-row. A of rank
- *            R is R pages holding its columns, B is R pages holding its rows; pages sit
- *            anywhere in one pool of num_pages x page_elems elements and are found through
- *            [num_slots][num_layers][r_max] page tables. Ranks differ per adapter and
- *            nothing is padded. Elements d_in.. / d_out.. of a page are never read.
+ *   paged    S-LoRA (arXiv 2311.03285) "Unified Paging": a page is one vector of
+ *            page_elems elements (one H-vector). A of rank R is R vectors of d_in elements
+ *            (its columns), B is R vectors of d_out elements (its rows); pages sit anywhere
+ *            in one pool of num_pages x page_elems elements. A vector longer than a page
+ *            spans ceil(d / page_elems) pages (d = d_in for A, d_out for B), so the page
+ *            tables are [num_slots][num_layers][r_max][ceil(d / page_elems)] int32: element
+ *            k of vector j is element k % page_elems of page table[..][j][k / page_elems].
+ *            With page_elems >= d this is one page per vector ([..][r_max][1]). Ranks differ
+ *            per adapter and nothing is padded. Page elements past a vector's end are never
+ *            read.
  *
  * CONVENTIONS FOR EVERY CALL
  *   - All array pointers are DEVICE pointers unless stated; the mlora_pool / mlora_problem
@@ -60,7 +65,7 @@
  *        offsets not 0 = off[0] <= ... <= off[n] = num_rows   -> BAD_OFFSETS, whole call skipped
  *        slot < -1 or slot >= num_slots                      -> BAD_SLOT, rows skipped
  *        rank[s] outside [1, r_max]                          -> BAD_RANK, rows skipped
- *        page id (j < rank[s]) outside [0, num_pages)        -> BAD_PAGE, rows skipped
+ *        a page id of a vector j < rank[s] outside [0, num_pages) -> BAD_PAGE, rows skipped
  *     A wait that exceeds its time limit inside a kernel sets MLORA_STATUS_TIMEOUT.
  *   - Slot -1 rows are never written (their y keeps its exact bits).
  *   - Calls whose outputs overlap on the device must be ordered by the caller (one stream).
@@ -117,13 +122,17 @@ typedef struct {
   const void *a_t;     /* stacked: A^T [num_slots][num_layers][r_max][d_in]  (NULL when paged) */
   const void *b;       /* stacked: B   [num_slots][num_layers][r_max][d_out] (NULL when paged) */
   const void *pages;   /* paged: [num_pages][page_elems]                     (NULL when stacked) */
-  int64_t page_elems;  /* paged: elements per page, >= max(d_in, d_out), multiple of 8 */
+  int64_t page_elems;  /* paged: elements per page, a multiple of 8, at least 8 */
   int64_t num_pages;   /* paged */
-  const int32_t *a_page_table; /* paged: [num_slots][num_layers][r_max], page of column j of A */
-  const int32_t *b_page_table; /* paged: [num_slots][num_layers][r_max], page of row j of B */
+  const int32_t *a_page_table; /* paged: [num_slots][num_layers][r_max][ceil(d_in/page_elems)], pages of column j of A */
+  const int32_t *b_page_table; /* paged: [num_slots][num_layers][r_max][ceil(d_out/page_elems)], pages of row j of B */
   const int32_t *rank;  /* [num_slots], each in [1, r_max] */
   const float *scale;   /* [num_slots], alpha / rank, applied by the expand */
 } mlora_pool;
+
+/* Launch flags of the _ex calls. */
+#define MLORA_LAUNCH_PROGRAMMATIC 1u /* programmatic dependent launch for this call (see
+                                        lora_set_programmatic_launch) */
 
 /* ---- two-phase form (Punica section 3.4: one shrink launch, one expand launch) --------- */
 
@@ -158,6 +167,25 @@ MLORA_API int lora_sgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const 
 
 MLORA_API int lora_bgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,
               int32_t num_rows, int32_t layer, float *v_scratch, int32_t *dev_status, void *stream);
+
+/* lora_bgmv with launch flags. Device-side grouping of the rows (Punica section 3.4, "Batch
+ * Layout Construction": rows that share an adapter form one group; "Multi-LoRA Serving, in
+ * depth", section "The decode cost model": each adapter read once per step): a first small
+ * kernel orders the rows by (rank descending, slot) on the GPU, the main kernel then walks the
+ * rows in that order. Rows of one adapter run side by side, so the adapter comes from HBM once;
+ * the heaviest rows start first. The caller's row order, x and y are unchanged; the order is
+ * kept in v_scratch (2 x num_rows int32). lora_bgmv groups batches of at least 128 rows (up to
+ * 4096 rows, r_max >= 2); the flags override that:
+ *   MLORA_LAUNCH_GROUP_ROWS   group (when num_rows <= 4096 and r_max >= 2)
+ *   MLORA_LAUNCH_NO_GROUPING  never group
+ *   MLORA_LAUNCH_PROGRAMMATIC programmatic dependent launch for the first kernel of the call
+ * Other bits are rejected with MLORA_ERR_SHAPE. Results are the same bits with or without
+ * grouping (every row's arithmetic is the same). */
+#define MLORA_LAUNCH_GROUP_ROWS 2u
+#define MLORA_LAUNCH_NO_GROUPING 4u
+MLORA_API int lora_bgmv_ex(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool,
+                           const int32_t *row_slot, int32_t num_rows, int32_t layer, float *v_scratch, uint32_t flags,
+                           int32_t *dev_status, void *stream);
 
 /* ---- fused form without a scratch argument -------------------------------------------------
  * lora_sgmv_noalloc: lora_sgmv for callers that cannot hand the library a device buffer --
@@ -204,9 +232,6 @@ typedef struct {
 MLORA_API int lora_sgmv_grouped(const mlora_problem *problems, int32_t num_problems, const int32_t *seg_offsets,
                       const int32_t *seg_slot, int32_t num_segments, int32_t num_rows, int32_t *dev_status,
                       void *stream);
-
-/* Launch flags of lora_sgmv_grouped_ex. */
-#define MLORA_LAUNCH_PROGRAMMATIC 1u /* programmatic dependent launch for this call (see below) */
 
 /* lora_sgmv_grouped with launch flags given per call instead of taken from the calling thread's
  * setting (lora_set_programmatic_launch). flags: 0 or MLORA_LAUNCH_PROGRAMMATIC; other bits are

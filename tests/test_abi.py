@@ -88,8 +88,8 @@ def expand(L, pool, y=Y, ldy=64, v=V, off=OFF, slot=SLOT, nseg=2, rows=8, layer=
     (dict(pool_kw=dict(a_t=0x10008)), m.ERR_ALIGN),
     (dict(pool_kw=dict(rank=0)), m.ERR_NULL),
     (dict(pool_kw=dict(kind=5)), m.ERR_POOL),
-    (dict(pool_kw=dict(kind=1, pages=0x50000, page_elems=32, num_pages=10, a_page_table=0x60000,
-                       b_page_table=0x70000)), m.ERR_POOL),  # page shorter than d_in
+    (dict(pool_kw=dict(kind=1, pages=0x50000, page_elems=0, num_pages=10, a_page_table=0x60000,
+                       b_page_table=0x70000)), m.ERR_POOL),  # empty pages (shorter pages than d are fine)
     (dict(pool_kw=dict(kind=1, pages=0x50000, page_elems=68, num_pages=10, a_page_table=0x60000,
                        b_page_table=0x70000)), m.ERR_ALIGN),
     (dict(pool_kw=dict(kind=1, pages=0, page_elems=64, num_pages=10, a_page_table=0x60000,

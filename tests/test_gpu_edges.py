@@ -25,7 +25,8 @@ def dev():
     return torch.device("cuda:0")
 
 
-def make_case(dev, seed, *, dtype, paged, r_max, d_in, d_out, M, num_slots=5, num_layers=2, max_seg=9):
+def make_case(dev, seed, *, dtype, paged, r_max, d_in, d_out, M, num_slots=5, num_layers=2, max_seg=9,
+              page_elems=None):
     rng = np.random.default_rng(seed)
     g = W.generator(seed, dev)
     ranks = rng.integers(1, r_max + 1, num_slots).astype(np.int32)
@@ -34,7 +35,7 @@ def make_case(dev, seed, *, dtype, paged, r_max, d_in, d_out, M, num_slots=5, nu
     if paged:
         pool = W.paged_pool(num_slots=num_slots, num_layers=num_layers, r_max=r_max, d_in=d_in, d_out=d_out,
                             dtype=dtype, gen=g, device=dev, rng=rng, ranks=ranks,
-                            page_elems=max(d_in, d_out) + 8 * int(rng.integers(0, 3)))
+                            page_elems=page_elems or max(d_in, d_out) + 8 * int(rng.integers(0, 3)))
     else:
         pool = W.stacked_pool(num_slots=num_slots, num_layers=num_layers, r_max=r_max, d_in=d_in, d_out=d_out,
                               dtype=dtype, gen=g, device=dev, ranks=ranks)
@@ -118,6 +119,68 @@ def test_fuzz_two_phase_and_fused(dev, shape, seed, form):
     check_op(op, batch, form, g2.y, g2.v, what="two-phase")
     check_op(op, batch, form, g1.y, what="fused")
 
+
+
+# S-LoRA "Unified Paging" with pages shorter than a vector: a rank-row of A^T (d_in) or B (d_out)
+# spans ceil(d / page_elems) pages at unrelated places of the pool. Shapes of the MLP projections
+# in hidden-size pages (gate/up: B rows of 11008 in 4096-element pages; down: A rows of 11008), and
+# odd splits: a CTA's slice of d_in or d_out, its staged B rows and its passes of A cross pages.
+SHORT_PAGES = [
+    # dtype, r_max, d_in, d_out, M, page_elems
+    (torch.bfloat16, 16, 4096, 11008, 32, 4096),
+    (torch.bfloat16, 16, 11008, 4096, 20, 4096),
+    (torch.float16, 64, 1032, 264, 130, 264),
+    (torch.bfloat16, 128, 520, 4104, 12, 136),
+    (torch.bfloat16, 64, 6000, 1000, 40, 1000),
+    (torch.float16, 8, 24, 520, 7, 8),
+]
+
+
+@pytest.mark.parametrize("shape", SHORT_PAGES, ids=lambda s: f"{'bf16' if s[0] == torch.bfloat16 else 'fp16'}-"
+                         f"r{s[1]}-{s[2]}x{s[3]}-M{s[4]}-pages{s[5]}")
+@pytest.mark.parametrize("form", ["sgmv", "bgmv"])
+def test_vectors_across_pages(dev, shape, form):
+    dtype, r_max, d_in, d_out, M, pe = shape
+    op, batch = make_case(dev, 300 + d_in, dtype=dtype, paged=True, r_max=r_max, d_in=d_in, d_out=d_out, M=M,
+                          page_elems=pe)
+    assert op.pool.a_page_table.shape[-1] == -(-d_in // pe) and op.pool.b_page_table.shape[-1] == -(-d_out // pe)
+    pool = m.make_pool(op.pool)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    g2, g1 = Guarded(op.y, r_max), Guarded(op.y, r_max)
+    if form == "sgmv":
+        m.lora_sgmv_shrink(g2.v, op.x, pool, batch.seg_offsets, batch.seg_slot, op.layer, st)
+        m.lora_sgmv_expand(g2.y, g2.v, pool, batch.seg_offsets, batch.seg_slot, op.layer, st)
+        m.lora_sgmv(g1.y, op.x, pool, batch.seg_offsets, batch.seg_slot, op.layer, g1.v, st)
+    else:
+        m.lora_bgmv_shrink(g2.v, op.x, pool, batch.row_slot, op.layer, st)
+        m.lora_bgmv_expand(g2.y, g2.v, pool, batch.row_slot, op.layer, st)
+        m.lora_bgmv(g1.y, op.x, pool, batch.row_slot, op.layer, g1.v, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    g2.check(True)
+    g1.check(False)
+    check_op(op, batch, form, g2.y, g2.v, what="two-phase, short pages")
+    check_op(op, batch, form, g1.y, what="fused, short pages")
+
+
+def test_bad_page_in_a_later_piece_of_a_vector(dev):
+    """A bad id in the second page of a vector is found like one in the first: BAD_PAGE, the
+    row untouched, the other rows correct."""
+    op, batch = make_case(dev, 9, dtype=torch.bfloat16, paged=True, r_max=8, d_in=64, d_out=48, M=8, num_slots=4,
+                          page_elems=24)
+    at = op.pool.a_page_table.clone()
+    at[2, op.layer, 0, 1] = op.pool.pages.shape[0]  # second of the three pages of slot 2's first A vector
+    p2 = W.Pool(op.pool.dtype, 4, op.pool.num_layers, 8, 64, 48, op.pool.rank, op.pool.scale, pages=op.pool.pages,
+                a_page_table=at, b_page_table=op.pool.b_page_table)
+    slots = torch.tensor([0, 1, 2, 3] * 2, dtype=torch.int32, device=dev)
+    y = op.y.clone()
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    m.lora_bgmv(y, op.x, m.make_pool(p2), slots, op.layer, new_v(8, 8, dev), st)
+    torch.cuda.synchronize()
+    assert st.item() == m.STATUS_BAD_PAGE
+    assert np.array_equal(bits(y)[2::4], bits(op.y)[2::4])
+    good = W.Batch(8, slots.cpu().masked_fill(slots.cpu() == 2, -1), None, None)
+    check_op(op, good.to(dev), "bgmv", y, what="rows of the other slots")
 
 
 # One-row tiles whose d_in slice spans several passes of A hold as few rank rows per warp as
@@ -282,3 +345,58 @@ def test_host_errors_launch_nothing(dev):
         m.lora_sgmv(op.y[:, 1:], op.x, op.pool, batch.seg_offsets, batch.seg_slot, 0, new_v(4, 8, dev))
     assert e.value.code in (m.ERR_ALIGN, m.ERR_SHAPE)
     assert m.launch_count() == before
+
+
+# Device-side grouping of BGMV rows (lora_bgmv_ex): the rows are walked in (rank descending, slot)
+# order computed on the GPU; the caller's rows, x and y stay in place, and every row's arithmetic
+# is the same, so grouped and ungrouped calls give the same bits.
+@pytest.mark.parametrize("paged", [False, True], ids=["stacked", "paged"])
+@pytest.mark.parametrize("M", [7, 200, 1500])
+def test_bgmv_row_grouping_same_bits_and_oracle(dev, paged, M):
+    rng = np.random.default_rng(M + paged)
+    g = W.generator(M, dev)
+    S = 60
+    ranks = rng.choice(np.array([1, 8, 16, 32, 64], np.int32), S)
+    kw = dict(num_slots=S, num_layers=1, r_max=64, d_in=1024, d_out=520, dtype=torch.bfloat16, gen=g, device=dev,
+              ranks=ranks)
+    pool = W.paged_pool(rng=rng, page_elems=512, **kw) if paged else W.stacked_pool(**kw)
+    slots = rng.choice(S, M, p=W.zipf_probs(S, 1.2)).astype(np.int32)
+    slots[::9] = -1
+    batch = W.batch_from_slots(slots, sgmv=False).to(dev)
+    x = W.normal((M, 1024), 1.0, torch.bfloat16, g, dev)
+    y0 = W.uniform((M, 520), -1, 1, torch.bfloat16, g, dev)
+    h = m.make_pool(pool)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs = {}
+    for name, flags in (("grouped", m.LAUNCH_GROUP_ROWS), ("plain", m.LAUNCH_NO_GROUPING), ("default", 0)):
+        y = y0.clone()
+        before = m.launch_count()
+        m.lora_bgmv_ex(y, x, h, batch.row_slot, 0, new_v(M, 64, dev), flags, st)
+        torch.cuda.synchronize()
+        launches = m.launch_count() - before
+        assert launches == (2 if flags == m.LAUNCH_GROUP_ROWS or (flags == 0 and M >= 128) else 1), name
+        outs[name] = y
+    assert st.item() == 0
+    assert np.array_equal(bits(outs["grouped"]), bits(outs["plain"])), "grouping changed the bits"
+    assert np.array_equal(bits(outs["default"]), bits(outs["plain"]))
+    check_op(W.Op("grouped", pool, 0, x, y0), batch, "bgmv", outs["grouped"], what="grouped BGMV")
+
+
+def test_bgmv_row_grouping_status_contract(dev):
+    """Invalid slots and ranks are still reported, and their rows left untouched, when the rows are
+    grouped (invalid rows sort last)."""
+    op, batch = make_case(dev, 5, dtype=torch.bfloat16, paged=False, r_max=16, d_in=64, d_out=48, M=12, num_slots=4)
+    rk = op.pool.rank.clone()
+    rk[1] = 0
+    p2 = W.Pool(op.pool.dtype, 4, op.pool.num_layers, 16, 64, 48, rk, op.pool.scale, a_t=op.pool.a_t, b=op.pool.b)
+    slots = torch.tensor([0, 9, -1, 1, -3, 2, 3, 0, 1, 2, 3, -1], dtype=torch.int32, device=dev)
+    y = op.y.clone()
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    m.lora_bgmv_ex(y, op.x, m.make_pool(p2), slots, op.layer, new_v(12, 16, dev), m.LAUNCH_GROUP_ROWS, st)
+    torch.cuda.synchronize()
+    assert st.item() == m.STATUS_BAD_SLOT | m.STATUS_BAD_RANK
+    for i in (1, 2, 3, 4, 8, 11):
+        assert np.array_equal(bits(y)[i], bits(op.y)[i])
+    good = slots.cpu().clone()
+    good[[1, 2, 3, 4, 8, 11]] = -1
+    check_op(op, W.Batch(12, good.to(dev), None, None), "bgmv", y, what="valid rows, grouped")

@@ -163,3 +163,84 @@ def test_mixed_prefill_and_decode_batch(dev, form):
     op = W.Op("mixed", pool, 0, x, y0)
     for y in outs:
         check_op(op, batch, "sgmv", y, v if form == "two_phase" else None, what=f"mixed batch {form}")
+
+
+# Paged pools on the tensor cores (S-LoRA "Unified Paging", MBGMM-style prefill over the pages):
+# the A^T / B rows of a tile are gathered from their pages; pages as long as a vector, and pages
+# shorter than a vector (one H-vector per page: 13B MLP rows of 13824 span three 5120-element
+# pages), with ranks differing per adapter.
+PAGED_CASES = [
+    # r_max, ranks, d_in, d_out, segment lengths, segment slots, page_elems (None: max(d_in, d_out))
+    (64, [64, 8, 33, 16], 5120, 640, [255, 130, 384, 3], [2, 0, 1, 3], None),
+    (64, [64, 8, 33, 16], 5120, 13824, [200, 129, 300], [1, 3, 0], 5120),
+    (32, [32, 1, 17], 13824, 5120, [128, 257, 5], [0, 2, 1], 5120),
+    (16, [16, 5, 16], 1024, 328, [31, 33, 64, 127, 200, 1], [0, 1, 2, 0, 1, 2], 96),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("case", PAGED_CASES, ids=lambda c: f"r{c[0]}-{c[2]}x{c[3]}-M{sum(c[4])}-pages{c[6]}")
+@pytest.mark.parametrize("mode", ["two_phase", "fused"])
+def test_prefill_tensor_core_path_paged(dev, case, mode, dtype):
+    r_max, ranks, d_in, d_out, lens, slots, pe = case
+    g = W.generator(13, dev)
+    rng = np.random.default_rng(13)
+    pool = W.paged_pool(num_slots=len(ranks), num_layers=2, r_max=r_max, d_in=d_in, d_out=d_out, dtype=dtype,
+                        gen=g, device=dev, rng=rng, ranks=ranks, page_elems=pe)
+    batch = W.batch_from_segments(lens, slots).to(dev)
+    x = W.normal((batch.M, d_in), 1.0, dtype, g, dev)
+    y0 = W.uniform((batch.M, d_out), -1, 1, dtype, g, dev)
+    op = W.Op("p", pool, 1, x, y0)
+    y, v = run_tc(dev, op, batch, mode, r_max)
+    check_op(op, batch, "sgmv", y, v if mode == "two_phase" else None, what=f"paged tc {mode}")
+
+
+def test_prefill_paged_13b_every_row(dev):
+    """Llama-2-13B shapes on a paged pool: 4 prompts of U[128, 700] rows, each on its own adapter
+    with ranks from {8, 16, 32, 64} (no padding to the largest), pages of one hidden-size vector
+    (5120 elements: the MLP rows of 13824 span three pages), all 7 projections of one layer
+    through the fused call; every row of every projection against the oracle."""
+    rng = np.random.default_rng(41)
+    g = W.generator(41, dev)
+    lens = rng.integers(128, 701, 4)
+    ranks = np.array([8, 16, 32, 64], np.int32)
+    batch = W.batch_from_segments(lens, [3, 0, 2, 1]).to(dev)
+    M = batch.M
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    x_h = W.normal((M, 5120), 1.0, torch.bfloat16, g, dev)
+    for proj in W.LLAMA2_13B:
+        pool = W.paged_pool(num_slots=4, num_layers=1, r_max=64, d_in=proj.d_in, d_out=proj.d_out,
+                            dtype=torch.bfloat16, gen=g, device=dev, rng=rng, ranks=ranks, page_elems=5120)
+        x = x_h if proj.d_in == 5120 else W.normal((M, proj.d_in), 1.0, torch.bfloat16, g, dev)
+        op = W.Op(proj.name, pool, 0, x, W.uniform((M, proj.d_out), -1, 1, torch.bfloat16, g, dev))
+        y = op.y.clone()
+        before = m.launch_count()
+        m.lora_sgmv(y, x, m.make_pool(pool), batch.seg_offsets, batch.seg_slot, 0, new_v(M, 64, dev), st)
+        torch.cuda.synchronize()
+        assert m.launch_count() - before == 3, f"{proj.name}: the tensor-core kernels did not run"
+        assert st.item() == 0
+        check_op(op, batch, "sgmv", y, what=f"paged 13B prefill {proj.name}")
+
+
+def test_prefill_paged_bad_page_reported(dev):
+    """A bad page id in a long segment's adapter: the tensor-core kernels report BAD_PAGE and leave
+    that segment's rows untouched; the other segments are correct."""
+    g = W.generator(14, dev)
+    rng = np.random.default_rng(14)
+    pool = W.paged_pool(num_slots=2, num_layers=1, r_max=16, d_in=256, d_out=264, dtype=torch.bfloat16, gen=g,
+                        device=dev, rng=rng, ranks=[16, 8], page_elems=128)
+    bt = pool.b_page_table.clone()
+    bt[1, 0, 3, 1] = -7  # second page of row 3 of slot 1's B
+    bad_pool = W.Pool(pool.dtype, 2, 1, 16, 256, 264, pool.rank, pool.scale, pages=pool.pages,
+                      a_page_table=pool.a_page_table, b_page_table=bt)
+    batch = W.batch_from_segments([300, 260], [0, 1]).to(dev)
+    x = W.normal((batch.M, 256), 1.0, torch.bfloat16, g, dev)
+    y0 = W.uniform((batch.M, 264), -1, 1, torch.bfloat16, g, dev)
+    y = y0.clone()
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    m.lora_sgmv(y, x, m.make_pool(bad_pool), batch.seg_offsets, batch.seg_slot, 0, new_v(batch.M, 16, dev), st)
+    torch.cuda.synchronize()
+    assert st.item() == m.STATUS_BAD_PAGE
+    assert torch.equal(y[300:].view(torch.int16), y0[300:].view(torch.int16))
+    good = W.Batch(batch.M, batch.row_slot.masked_fill(batch.row_slot == 1, -1), None, None)
+    check_op(W.Op("p", pool, 0, x, y0), good, "bgmv", y, what="segment with good pages")

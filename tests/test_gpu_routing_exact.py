@@ -50,7 +50,8 @@ def b_value(s, layer, n):
     return 2.0 ** -(2 + (s + layer) % 3) * (1 + n % 3)
 
 
-def exact_pool(dev, dtype, *, num_slots, num_layers, r_max, d_in, d_out, ranks, paged, rng, page_pad=0):
+def exact_pool(dev, dtype, *, num_slots, num_layers, r_max, d_in, d_out, ranks, paged, rng, page_pad=0,
+               page_elems=None):
     ranks = np.asarray(ranks, np.int32)
     a_t = torch.empty((num_slots, num_layers, r_max, d_in), dtype=torch.float32)
     b = torch.empty((num_slots, num_layers, r_max, d_out), dtype=torch.float32)
@@ -68,24 +69,25 @@ def exact_pool(dev, dtype, *, num_slots, num_layers, r_max, d_in, d_out, ranks, 
     if not paged:
         return W.Pool(dtype, num_slots, num_layers, r_max, d_in, d_out, rank_t, scale_t,
                       a_t=a_t.to(dev), b=b.to(dev))
-    # the same adapters in pages at permuted positions, free pages (NaN) interleaved
-    page_elems = max(d_in, d_out) + page_pad
-    used = int(2 * num_layers * ranks.sum())
+    # the same adapters in pages at permuted positions, free pages (NaN) interleaved; with
+    # page_elems below d a vector is cut into ceil(d / page_elems) pages placed independently
+    page_elems = max(d_in, d_out) + page_pad if page_elems is None else page_elems
+    a_ppv, b_ppv = -(-d_in // page_elems), -(-d_out // page_elems)
+    used = int(num_layers * ranks.sum() * (a_ppv + b_ppv))
     num_pages = used + used // 4 + 3
-    phys = rng.permutation(num_pages)[:used]
+    phys = iter(rng.permutation(num_pages)[:used])
     pages = torch.full((num_pages, page_elems), float("nan"), dtype=dtype)
-    a_tab = np.full((num_slots, num_layers, r_max), -1, np.int32)
-    b_tab = np.full((num_slots, num_layers, r_max), -1, np.int32)
-    q = 0
+    a_tab = np.full((num_slots, num_layers, r_max, a_ppv), -1, np.int32)
+    b_tab = np.full((num_slots, num_layers, r_max, b_ppv), -1, np.int32)
     for s in range(num_slots):
         for layer in range(num_layers):
             for j in range(ranks[s]):
-                a_tab[s, layer, j] = phys[q]
-                pages[phys[q], :d_in] = a_t[s, layer, j]
-                q += 1
-                b_tab[s, layer, j] = phys[q]
-                pages[phys[q], :d_out] = b[s, layer, j]
-                q += 1
+                for tab, src, d, n in ((a_tab, a_t, d_in, a_ppv), (b_tab, b, d_out, b_ppv)):
+                    for q in range(n):
+                        pg = next(phys)
+                        tab[s, layer, j, q] = pg
+                        lo, hi = q * page_elems, min(d, (q + 1) * page_elems)
+                        pages[pg, :hi - lo] = src[s, layer, j, lo:hi]
     return W.Pool(dtype, num_slots, num_layers, r_max, d_in, d_out, rank_t, scale_t, pages=pages.to(dev),
                   a_page_table=torch.from_numpy(a_tab).to(dev), b_page_table=torch.from_numpy(b_tab).to(dev))
 
@@ -152,21 +154,26 @@ DECODE_CASES = [
     (torch.bfloat16, False, 64, 6000, 1000, 200, 200, [1, 8, 16, 32, 33, 64]),  # rank-aware layouts
     (torch.bfloat16, True, 128, 7168, 520, 160, 160, [1, 9, 33, 64, 65, 128]),  # rank-aware, paged
     (torch.bfloat16, False, 128, 4104, 2056, 21, 4, [128, 1, 77, 128, 3, 64]),  # generic multi-row path
+    # pages shorter than the vectors (S-LoRA: a page is one H-vector; MLP rows span several)
+    (torch.bfloat16, True, 16, 4096, 11008, 32, 32, [16, 1, 7, 16, 3, 12], 4096),
+    (torch.float16, True, 32, 11008, 4096, 24, 6, [32, 1, 17, 8, 32, 4], 4096),
+    (torch.bfloat16, True, 64, 6000, 1000, 200, 200, [1, 8, 16, 32, 33, 64], 1000),
 ]
 
 
 def ids(c):
     return (f"{'bf16' if c[0] == torch.bfloat16 else 'fp16'}-{'paged' if c[1] else 'stacked'}-r{c[2]}-"
-            f"{c[3]}x{c[4]}-M{c[5]}-n{c[6]}")
+            f"{c[3]}x{c[4]}-M{c[5]}-n{c[6]}" + (f"-pages{c[8]}" if len(c) > 8 else ""))
 
 
 @pytest.mark.parametrize("case", DECODE_CASES, ids=ids)
 def test_exact_routing_decode_kernels(dev, case):
-    dtype, paged, r_max, d_in, d_out, M, nseg, ranks = case
+    dtype, paged, r_max, d_in, d_out, M, nseg, ranks = case[:8]
+    page_elems = case[8] if len(case) > 8 else None
     rng = np.random.default_rng(zlib.crc32(ids(case).encode()))
     num_layers = 2
     pool = exact_pool(dev, dtype, num_slots=len(ranks), num_layers=num_layers, r_max=r_max, d_in=d_in, d_out=d_out,
-                      ranks=ranks, paged=paged, rng=rng, page_pad=8 * int(rng.integers(0, 3)))
+                      ranks=ranks, paged=paged, rng=rng, page_pad=8 * int(rng.integers(0, 3)), page_elems=page_elems)
     h = m.make_pool(pool)
     layer = 1
     st = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -219,13 +226,17 @@ TC_CASES = [
 ]
 
 
+@pytest.mark.parametrize("pages", [None, "square", "short"])
 @pytest.mark.parametrize("case", TC_CASES, ids=lambda c: f"{'bf16' if c[0] == torch.bfloat16 else 'fp16'}-r{c[1]}-"
                          f"{c[2]}x{c[3]}-M{sum(c[4])}")
-def test_exact_routing_tensor_core_path(dev, case):
+def test_exact_routing_tensor_core_path(dev, case, pages):
+    """pages: stacked pool (None), paged with a page per vector, paged with pages of about a third
+    of the longer vector (vectors span two to four pages; page boundaries fall inside atoms)."""
     dtype, r_max, d_in, d_out, lens, slots, ranks = case
     rng = np.random.default_rng(sum(lens))
+    short = max(64, (max(d_in, d_out) // 3 + 7) // 8 * 8)
     pool = exact_pool(dev, dtype, num_slots=len(ranks), num_layers=2, r_max=r_max, d_in=d_in, d_out=d_out,
-                      ranks=ranks, paged=False, rng=rng)
+                      ranks=ranks, paged=pages is not None, rng=rng, page_elems=short if pages == "short" else None)
     h = m.make_pool(pool)
     off = np.r_[0, np.cumsum(lens)].astype(np.int32)
     seg_slot = np.asarray(slots, np.int32)

@@ -56,7 +56,8 @@ class Pool:
     stacked: a_t [num_slots][num_layers][r_max][d_in] (rows of A^T = columns of A) and
              b   [num_slots][num_layers][r_max][d_out] (rows of B).
     paged:   pages [num_pages][page_elems]; a_page_table / b_page_table
-             [num_slots][num_layers][r_max] int32 page ids (-1 where j >= rank).
+             [num_slots][num_layers][r_max][ceil(d / page_elems)] int32 page ids (-1 where
+             j >= rank): a vector longer than a page spans several.
     rank int32 [num_slots], scale float32 [num_slots].
     """
     dtype: torch.dtype
@@ -233,34 +234,40 @@ def stacked_pool(*, num_slots, num_layers, r_max, d_in, d_out, dtype, gen, devic
 def paged_pool(*, num_slots, num_layers, r_max, d_in, d_out, dtype, gen, device, rng: np.random.Generator,
                ranks, page_elems: Optional[int] = None, free_fraction: float = 0.10, alpha: float = 32.0,
                a_var: Optional[float] = None, b_var: float = 0.02) -> Pool:
-    """S-LoRA-style paged pool: every rank-row of A^T and of B is one page of `page_elems`
-    elements at a random physical position; about `free_fraction` of the pages are free and
-    hold NaNs, interleaved with the used ones. Elements of a page past d_in (or d_out) are NaN."""
+    """S-LoRA-style paged pool: every rank-row of A^T and of B is stored in pages of `page_elems`
+    elements at random physical positions; about `free_fraction` of the pages are free and hold
+    NaNs, interleaved with the used ones. A vector longer than a page (page_elems < d) spans
+    ceil(d / page_elems) pages, each placed on its own; page tables are
+    [num_slots][num_layers][r_max][ceil(d / page_elems)] (-1 where j >= rank). Elements of a page
+    past the vector's end are NaN."""
     ranks = np.asarray(ranks, np.int32)
     page_elems = max(d_in, d_out) if page_elems is None else page_elems
-    used = int(2 * num_layers * ranks.sum())
+    a_ppv, b_ppv = -(-d_in // page_elems), -(-d_out // page_elems)
+    used = int(num_layers * ranks.sum() * (a_ppv + b_ppv))
     num_pages = int(math.ceil(used * (1.0 + free_fraction)))
     phys = rng.permutation(num_pages)[:used].astype(np.int32)
-    a_tab = np.full((num_slots, num_layers, r_max), -1, np.int32)
-    b_tab = np.full((num_slots, num_layers, r_max), -1, np.int32)
+    a_tab = np.full((num_slots, num_layers, r_max, a_ppv), -1, np.int32)
+    b_tab = np.full((num_slots, num_layers, r_max, b_ppv), -1, np.int32)
     q = 0
     for s in range(num_slots):
         r = int(ranks[s])
         for layer in range(num_layers):
-            a_tab[s, layer, :r] = phys[q:q + r]
-            q += r
-            b_tab[s, layer, :r] = phys[q:q + r]
-            q += r
+            a_tab[s, layer, :r] = phys[q:q + r * a_ppv].reshape(r, a_ppv)
+            q += r * a_ppv
+            b_tab[s, layer, :r] = phys[q:q + r * b_ppv].reshape(r, b_ppv)
+            q += r * b_ppv
     pages = torch.empty((num_pages, page_elems), dtype=dtype, device=device)
     poison_(pages)
     a_var = 1.0 / d_in if a_var is None else a_var
-    a_ids = torch.from_numpy(a_tab[a_tab >= 0].astype(np.int64)).to(device)
-    b_ids = torch.from_numpy(b_tab[b_tab >= 0].astype(np.int64)).to(device)
-    chunk = max(1, (1 << 26) // page_elems)
-    for ids, d, var in ((a_ids, d_in, a_var), (b_ids, d_out, b_var)):
-        for s in range(0, ids.numel(), chunk):
-            sel = ids[s:s + chunk]
-            pages[sel, :d] = normal((sel.numel(), d), var, dtype, gen, device)
+    for tab, d, var in ((a_tab, d_in, a_var), (b_tab, d_out, b_var)):
+        vecs = tab[tab[..., 0] >= 0]  # [vectors][ppv] page ids, in table order
+        chunk = max(1, (1 << 26) // d)
+        for s0 in range(0, vecs.shape[0], chunk):
+            sel = vecs[s0:s0 + chunk]
+            vals = normal((sel.shape[0], d), var, dtype, gen, device)
+            for q in range(sel.shape[1]):  # piece q of every vector goes to its own page
+                lo, hi = q * page_elems, min(d, (q + 1) * page_elems)
+                pages[torch.from_numpy(sel[:, q].astype(np.int64)).to(device), :hi - lo] = vals[:, lo:hi]
     scales = (alpha / ranks.astype(np.float64)).astype(np.float32)
     return Pool(dtype, num_slots, num_layers, r_max, d_in, d_out,
                 torch.from_numpy(ranks).to(device), torch.from_numpy(scales).to(device),
