@@ -75,9 +75,17 @@ mlora::PoolDev to_dev(const mlora_pool *p) {
   d.rank = p->rank;
   d.scale = p->scale;
   d.a_ppv = d.b_ppv = 1;
+  d.pe_mul = 1;
+  d.pe_shift = 0;
   if (p->kind == MLORA_POOL_PAGED) {  // a vector longer than a page spans several
     d.a_ppv = (int32_t)((p->d_in + p->page_elems - 1) / p->page_elems);
     d.b_ppv = (int32_t)((p->d_out + p->page_elems - 1) / p->page_elems);
+    // division by page_elems as a multiply-high and a shift (Granlund and Montgomery, 1994)
+    const uint64_t pe = (uint64_t)p->page_elems;
+    int l = 0;
+    while ((1ull << l) < pe) ++l;
+    d.pe_mul = (uint32_t)(((1ull << 32) * ((1ull << l) - pe)) / pe + 1);
+    d.pe_shift = l;
   }
   return d;
 }

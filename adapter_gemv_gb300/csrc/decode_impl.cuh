@@ -65,11 +65,20 @@ struct TileInfo {
 // A paged vector spans ppv consecutive page-table entries: element k sits in entry
 // k / page_elems at offset k % page_elems (a chunk of 8 elements never straddles two pages:
 // page_elems is a multiple of 8). Square pages (ppv == 1) take one table entry per vector.
+// Page of element k (k < 2^31) of a multi-page vector: k / page_elems by one multiply-high and a
+// shift with the host's pe_mul / pe_shift (T. Granlund and P. Montgomery, "Division by Invariant
+// Integers using Multiplication", 1994: q = (mulhi(m, k) + k) >> l, l = ceil(log2 d),
+// m = floor(2^32 (2^l - d) / d) + 1).
+__device__ __forceinline__ int page_of(const PoolDev &pl, int k) {
+  return (int)((__umulhi((uint32_t)k, pl.pe_mul) + (uint32_t)k) >> pl.pe_shift);
+}
+
+// Branch-free, so that a batch of such addresses issues its table loads together (for one-page
+// vectors q is 0).
 __device__ __forceinline__ const uint16_t *paged_elem(const PoolDev &pl, const int32_t *tab, int ppv, int64_t t,
                                                       int k) {
-  if (ppv == 1) return pl.pages + (int64_t)tab[t] * pl.page_elems + k;
-  const int pe = (int)pl.page_elems, q = k / pe;
-  return pl.pages + (int64_t)tab[t * ppv + q] * pl.page_elems + (k - q * pe);
+  const int q = page_of(pl, k);
+  return pl.pages + (int64_t)tab[t * ppv + q] * pl.page_elems + (k - q * (int)pl.page_elems);
 }
 
 __device__ __forceinline__ const uint16_t *a_elem(const PoolDev &pl, int s, int layer, int j, int k) {
@@ -84,6 +93,37 @@ __device__ __forceinline__ const uint16_t *b_elem(const PoolDev &pl, int s, int 
   return paged_elem(pl, pl.b_tab, pl.b_ppv, t, n);
 }
 
+// Element n of the B rows of one slot and layer, for a batch of rank rows: the slot/layer part of
+// the address and n's page are worked out once; row j then costs a multiply-add (and, paged, one
+// page-table read).
+struct BRows {
+  const uint16_t *base;  // stacked: &B[s][layer][0][n]; paged: the pool
+  const int32_t *tab;    // paged: the page-table entry of row 0's piece that holds n
+  int64_t stride;        // stacked: d_out; paged: page_elems
+  int32_t ppv, off;      // paged: table entries per row, n's offset in its page
+  bool paged;
+  __device__ __forceinline__ BRows(const PoolDev &pl, int s, int layer, int n) {
+    const int64_t t0 = ((int64_t)s * pl.num_layers + layer) * pl.r_max;
+    paged = pl.kind != MLORA_POOL_STACKED;
+    if (!paged) {
+      base = pl.b + t0 * pl.d_out + n;
+      stride = pl.d_out;
+      tab = nullptr;
+      ppv = off = 0;
+    } else {
+      const int q = page_of(pl, n);
+      base = pl.pages;
+      stride = pl.page_elems;
+      ppv = pl.b_ppv;
+      tab = pl.b_tab + t0 * pl.b_ppv + q;
+      off = n - q * (int)pl.page_elems;
+    }
+  }
+  __device__ __forceinline__ const uint16_t *operator()(int j) const {
+    return paged ? base + (int64_t)tab[j * ppv] * stride + off : base + (int64_t)j * stride;
+  }
+};
+
 // f(ptr, off, count) for each piece of elements [k0, k1) of a vector that lies in one page (the
 // whole range for a stacked pool or square pages); off is the piece's first element minus k0.
 template <bool IS_A, class F>
@@ -94,8 +134,9 @@ __device__ __forceinline__ void vec_pieces(const PoolDev &pl, int s, int layer, 
     return;
   }
   const int pe = (int)pl.page_elems;
+#pragma unroll 1
   for (int k = k0; k < k1;) {
-    const int end = min(k1, (k / pe + 1) * pe);
+    const int end = min(k1, (page_of(pl, k) + 1) * pe);
     f(IS_A ? a_elem(pl, s, layer, j, k) : b_elem(pl, s, layer, j, k), k - k0, end - k);
     k = end;
   }
@@ -264,17 +305,20 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
         } else if (pl.kind == MLORA_POOL_PAGED) {
           const int64_t t0 = ((int64_t)s * pl.num_layers + pr.layer) * pl.r_max;
           int32_t badp = 0;
-          // every page of every vector j < rank this mode reads
-          if (MODE != MODE_EXPAND)
-            for (int e = lane; e < rank * pl.a_ppv; e += 32) {
-              const int32_t pg = pl.a_tab[t0 * pl.a_ppv + e];
-              badp |= (pg < 0 || pg >= pl.num_pages);
+          // every page of every vector j < rank this mode reads: entries [0, na) of the A table's
+          // rows, then [na, na + nb) of the B table's, four loads in flight per lane at a time
+          const int na = MODE != MODE_EXPAND ? rank * pl.a_ppv : 0;
+          const int nt = na + (MODE != MODE_SHRINK ? rank * pl.b_ppv : 0);
+          for (int e0 = lane; e0 < nt; e0 += 128) {
+            int32_t pg[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int e = e0 + 32 * u;
+              pg[u] = e >= nt ? 0 : e < na ? pl.a_tab[t0 * pl.a_ppv + e] : pl.b_tab[t0 * pl.b_ppv + (e - na)];
             }
-          if (MODE != MODE_SHRINK)
-            for (int e = lane; e < rank * pl.b_ppv; e += 32) {
-              const int32_t pg = pl.b_tab[t0 * pl.b_ppv + e];
-              badp |= (pg < 0 || pg >= pl.num_pages);
-            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) badp |= (pg[u] < 0 || pg[u] >= pl.num_pages);
+          }
           if (__any_sync(0xffffffffu, badp)) bad = MLORA_STATUS_BAD_PAGE;
         }
       }
@@ -745,6 +789,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       for (int j = 0; j < RV; ++j) vr[j] = (VREG && j < rank) ? vsm[j] : 0.f;
       for (int c8 = tid; c8 < n8; c8 += NTHREADS) {
         const int n0 = n_begin + c8 * 8;
+        const BRows brow(pl, s, pr.layer, n0);
         float2 ev[4], od[4];  // even / odd rank rows
 #pragma unroll
         for (int e = 0; e < 4; ++e) ev[e] = od[e] = make_float2(0.f, 0.f);
@@ -777,7 +822,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
               uint4 bq[UB];
               if (j0 + UB <= rank) {  // a whole batch of rank rows: no guards
 #pragma unroll
-                for (int u = 0; u < UB; ++u) bq[u] = ldg_stream(b_elem(pl, s, pr.layer, j0 + u, n0), evict_first);
+                for (int u = 0; u < UB; ++u) bq[u] = ldg_stream(brow(j0 + u), evict_first);
 #pragma unroll
                 for (int u = 0; u < UB; u += 2) {
                   add_row(bq[u], vr[j0 + u], ev);
@@ -786,7 +831,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
               } else if (j0 < rank) {
 #pragma unroll
                 for (int u = 0; u < UB; ++u)
-                  if (j0 + u < rank) bq[u] = ldg_stream(b_elem(pl, s, pr.layer, j0 + u, n0), evict_first);
+                  if (j0 + u < rank) bq[u] = ldg_stream(brow(j0 + u), evict_first);
 #pragma unroll
                 for (int u = 0; u < UB; u += 2) {
                   if (j0 + u < rank) add_row(bq[u], vr[j0 + u], ev);
@@ -807,7 +852,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
               uint4 bq[UB];
               if (j0 + UB <= rank) {  // a whole batch of rank rows: no guards
 #pragma unroll
-                for (int u = 0; u < UB; ++u) bq[u] = ldg_stream(b_elem(pl, s, pr.layer, j0 + u, n0), evict_first);
+                for (int u = 0; u < UB; ++u) bq[u] = ldg_stream(brow(j0 + u), evict_first);
 #pragma unroll
                 for (int u = 0; u < UB; u += 2) {
                   add_row(bq[u], vsm[j0 + u], ev);
@@ -816,7 +861,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
               } else {
 #pragma unroll
                 for (int u = 0; u < UB; ++u)
-                  if (j0 + u < rank) bq[u] = ldg_stream(b_elem(pl, s, pr.layer, j0 + u, n0), evict_first);
+                  if (j0 + u < rank) bq[u] = ldg_stream(brow(j0 + u), evict_first);
 #pragma unroll
                 for (int u = 0; u < UB; u += 2) {
                   if (j0 + u < rank) add_row(bq[u], vsm[j0 + u], ev);
@@ -841,6 +886,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       // broadcast read of shared memory) in paired fp32 FMAs.
       for (int c8 = tid; c8 < n8; c8 += NTHREADS) {
         const int n0 = n_begin + c8 * 8;
+        const BRows brow(pl, s, pr.layer, n0);
         float2 acc2[RT][4];
 #pragma unroll
         for (int i = 0; i < RT; ++i)
@@ -870,7 +916,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
             uint4 b[UB];
 #pragma unroll
             for (int u = 0; u < UB; ++u)
-              if (j0 + u < rank) b[u] = ldg_stream(b_elem(pl, s, pr.layer, j0 + u, n0), evict_first);
+              if (j0 + u < rank) b[u] = ldg_stream(brow(j0 + u), evict_first);
 #pragma unroll
             for (int u = 0; u < UB; ++u)
               if (j0 + u < rank) add_row(b[u], j0 + u);

@@ -44,7 +44,12 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
   // adapters, BGMV), else 4 (an adapter row is reused across 4 rows; measured faster than 8 on
   // decode steps, whose longer tiles cost more registers and more empty rows).
   const bool sgmv = p.seg_off != nullptr;
-  const bool multi = sgmv && p.M >= 2 * (p.nseg > 0 ? p.nseg : 1);
+  // When the tensor-core kernels take the long segments (a prefill or mixed batch), the segments
+  // left here are short -- in a mixed batch, the one-row segments of decode requests -- so the
+  // batch's average segment length says nothing about them: one-row tiles.
+  bool tc_split = false;
+  for (int q = 0; q < p.nprob; ++q) tc_split |= p.prob[q].tc_min > 0;
+  const bool multi = sgmv && !tc_split && p.M >= 2 * (p.nseg > 0 ? p.nseg : 1);
   p.rt = multi ? 4 : 1;
   const int64_t all_tiles =
       !sgmv ? (int64_t)p.M : (p.rt == 1 ? (int64_t)p.M : (int64_t)p.nseg + (p.M + p.rt - 1) / p.rt);

@@ -15,6 +15,8 @@ struct PoolDev {
   const int32_t *a_tab, *b_tab, *rank;  // paged: [slot][layer][r_max][a_ppv or b_ppv] page ids
   const float *scale;
   int32_t a_ppv, b_ppv;  // paged: pages per vector, ceil(d_in / page_elems), ceil(d_out / page_elems)
+  uint32_t pe_mul;       // paged: k / page_elems = (mulhi(pe_mul, k) + k) >> pe_shift for k < 2^31
+  int32_t pe_shift;
 };
 
 enum { MODE_SHRINK = 0, MODE_EXPAND = 1, MODE_FUSED = 2 };

@@ -616,7 +616,9 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
     __syncwarp();
   } else if (active && warp == EXP_EPI_WARPS + 2) {
     // ---- store (one lane): each finished y tile goes out by TMA; its buffer is freed once the
-    // store has read it (a partial tile was written by the epilogue with plain stores)
+    // store has read it (a partial tile was written by the epilogue with plain stores). One store
+    // at a time: freeing a buffer a block later (two stores in flight) shortens the load ring,
+    // and loads are what limits this kernel (7 expands of the 13B prefill 723 -> 834 us).
     if (lane == 0) {
       for (int i = 0; i < nblk; ++i) {
         if (!mbar_wait(&ystaged[i % EBUF], (uint32_t)(i / EBUF) & 1u)) {

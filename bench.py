@@ -466,22 +466,43 @@ def config_fractions(dev, stream, peak, iters=30):
                                       "frac": round(by / t / 1e9 / peak, 4), "launches": plan.launches}
         del w, plan, g
         torch.cuda.empty_cache()
-    w = W.sgmv_prefill_13b(device=dev)
-    tot_t, tot_b, tot_f = 0.0, 0, 0
-    for op in w.ops:
-        h = m.make_pool(op.pool)
-        v = torch.empty((w.batch.M, op.pool.r_max), dtype=torch.float32, device=dev)
-        fn = lambda s, op=op, h=h, v=v: m.lora_sgmv(op.y, op.x, h, w.batch.seg_offsets, w.batch.seg_slot, 0, v,
-                                                     stream=s)
-        tot_t += time_calls(fn, stream, 5, flush)
-        tot_b += op_bytes_of(op, w.batch)
-        tot_f += op_flops_of(op, w.batch)
-    res["4_prefill_13b"] = {"us_7_ops": round(tot_t * 1e6, 1), "bytes": tot_b, "gbs": round(tot_b / tot_t / 1e9, 1),
-                            "frac": round(tot_b / tot_t / 1e9 / peak, 4), "rows": w.batch.M,
-                            "flops": tot_f, "tensor": tensor_fraction(tot_f, tot_t)}
-    del w
+    def seven_ops(name, w):
+        """The 7 projections of a prefill-sized batch, one fused call each (L2 flushed per call)."""
+        tot_t, tot_b, tot_f = 0.0, 0, 0
+        for op in w.ops:
+            h = m.make_pool(op.pool)
+            v = torch.empty((w.batch.M, op.pool.r_max), dtype=torch.float32, device=dev)
+            fn = lambda s, op=op, h=h, v=v: m.lora_sgmv(op.y, op.x, h, w.batch.seg_offsets, w.batch.seg_slot, 0, v,
+                                                         stream=s)
+            tot_t += time_calls(fn, stream, 5, flush)
+            tot_b += op_bytes_of(op, w.batch)
+            tot_f += op_flops_of(op, w.batch)
+        res[name] = {"us_7_ops": round(tot_t * 1e6, 1), "bytes": tot_b, "gbs": round(tot_b / tot_t / 1e9, 1),
+                     "frac": round(tot_b / tot_t / 1e9 / peak, 4), "rows": w.batch.M, "segments": int(w.batch.seg_slot.numel()),
+                     "flops": tot_f, "tensor": tensor_fraction(tot_f, tot_t)}
+
+    seven_ops("4_prefill_13b", W.sgmv_prefill_13b(device=dev))
+    torch.cuda.empty_cache()
+    seven_ops("6_mixed_prefill_decode_13b", W.mixed_prefill_decode_13b(device=dev))
     torch.cuda.empty_cache()
     single("5_paged_hetero_70b", W.paged_decode_70b(device=dev), "bgmv")
+    # the same pool with 2048 rows: the adapters the rows use (about 1.1 GB) exceed L2, so reading
+    # each once per call needs the rows grouped by adapter (device-side grouping, lora_bgmv's default
+    # from 128 rows) -- timed with and without it
+    w = W.paged_decode_70b(device=dev, M=2048)
+    op = w.ops[0]
+    h = m.make_pool(op.pool)
+    v = torch.empty((w.batch.M, op.pool.r_max), dtype=torch.float32, device=dev)
+    by = op_bytes_of(op, w.batch)
+    out = {}
+    for label, fl in (("grouped", m.LAUNCH_GROUP_ROWS), ("ungrouped", m.LAUNCH_NO_GROUPING)):
+        t = time_calls(lambda s, fl=fl: m.lora_bgmv_ex(op.y, op.x, h, w.batch.row_slot, 0, v, fl, stream=s), stream,
+                       10, flush)
+        out[label] = {"us": round(t * 1e6, 1), "bytes": by, "gbs": round(by / t / 1e9, 1),
+                      "frac": round(by / t / 1e9 / peak, 4)}
+    res["5b_paged_70b_2048_rows"] = out
+    del w, op, h, v
+    torch.cuda.empty_cache()
     return res
 
 

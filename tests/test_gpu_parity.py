@@ -176,3 +176,41 @@ def test_paged_hetero_rank_70b(dev, mode):
     torch.cuda.synchronize()
     assert st.item() == 0
     check_op(w.ops[0], w.batch, "bgmv", y, v, what=f"paged 70b {mode}")
+
+
+def test_mixed_prefill_decode_13b_sampled(dev):
+    """The bench's mixed batch (Punica's batch layout: 3 prompts of 300-2000 rows, then 64 one-row
+    decode segments on their own adapters; Llama-2-13B shapes, r = 64), all 7 projections through
+    the fused call: the prompts on the tensor cores, the decode rows on the CUDA-core kernel. The
+    oracle checks every decode row and rows at both sides of every prompt's 128-row blocks."""
+    w = W.mixed_prefill_decode_13b(device=dev)
+    off = w.batch.seg_offsets.cpu().numpy()
+    rows = np.unique(np.r_[prefill_sample_rows(W.Batch(int(off[3]), w.batch.row_slot[:off[3]],
+                                                       w.batch.seg_offsets[:4], w.batch.seg_slot[:3])),
+                           np.arange(off[3], w.batch.M)])
+    st = status_of(dev)
+    for op in w.ops:
+        before = m.launch_count()
+        y, _ = run_op(op, w.batch, "sgmv", "fused", st)
+        torch.cuda.synchronize()
+        assert m.launch_count() - before == 3, "the prompts did not run on the tensor cores"
+        check_op(op, w.batch, "sgmv", y, rows=rows, what=f"mixed 13B {op.name}")
+    assert st.item() == 0
+
+
+def test_paged_70b_2048_rows_grouped_sampled(dev):
+    """2048 rows over the 2000-adapter paged pool (the adapters used exceed L2): lora_bgmv groups
+    the rows on the device; every 8th row against the oracle, and the bits equal the ungrouped
+    call's."""
+    w = W.paged_decode_70b(device=dev, M=2048)
+    op = w.ops[0]
+    h = m.make_pool(op.pool)
+    st = status_of(dev)
+    y_g, y_p = op.y.clone(), op.y.clone()
+    v = torch.empty((2048, op.pool.r_max), dtype=torch.float32, device=dev)
+    m.lora_bgmv_ex(y_g, op.x, h, w.batch.row_slot, 0, v, m.LAUNCH_GROUP_ROWS, st)
+    m.lora_bgmv_ex(y_p, op.x, h, w.batch.row_slot, 0, v, m.LAUNCH_NO_GROUPING, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(bits(y_g), bits(y_p))
+    check_op(op, w.batch, "bgmv", y_g, rows=np.arange(0, 2048, 8), what="paged 70B 2048 rows grouped")

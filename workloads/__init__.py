@@ -397,3 +397,28 @@ def paged_decode_70b(device="cpu", seed=5, M=256, num_adapters=2000, d=8192, ran
     y = uniform((M, d), -1, 1, dt, g, device)
     return Workload(f"paged_bgmv_llama2_70b_q_proj_bs{M}_{num_adapters}_adapters", dt, batch,
                     [Op("q", pool, 0, x, y)], "bgmv", [pool])
+
+
+def mixed_prefill_decode_13b(device="cpu", seed=6, r=64, prompts=(300, 1200, 2000), decode_rows=64,
+                             projections: Sequence[Projection] = LLAMA2_13B) -> Workload:
+    """bf16 mixed batch in Punica's batch layout (section 3.4, "Batch Layout Construction"): the
+    prompts of new requests first, one segment and adapter each, then `decode_rows` one-row decode
+    segments, each request on its own adapter; Llama-2-13B shapes, all seven projections of one
+    layer, r = 64, scale 32/64. The prompts are long segments (the tensor-core kernels), the decode
+    rows short ones (the CUDA-core kernel), in one SGMV call per projection."""
+    g = generator(seed, device)
+    dt = torch.bfloat16
+    n_adapters = len(prompts) + decode_rows
+    lens = np.r_[np.asarray(prompts, np.int64), np.ones(decode_rows, np.int64)]
+    batch = batch_from_segments(lens, np.arange(n_adapters)).to(device)
+    M = batch.M
+    pools = {p.name: stacked_pool(num_slots=n_adapters, num_layers=1, r_max=r, d_in=p.d_in, d_out=p.d_out,
+                                  dtype=dt, gen=g, device=device) for p in projections}
+    hidden = projections[0].d_in
+    x_shared = normal((M, hidden), 1.0, dt, g, device)
+    x_o = normal((M, hidden), 1.0, dt, g, device)
+    ops = []
+    for p in projections:
+        x = x_o if p.name == "o" else normal((M, p.d_in), 1.0, dt, g, device) if p.name == "down" else x_shared
+        ops.append(Op(p.name, pools[p.name], 0, x, uniform((M, p.d_out), -1, 1, dt, g, device)))
+    return Workload(f"mixed_prefill_decode_llama2_13b_r{r}_M{M}", dt, batch, ops, "sgmv", list(pools.values()))
