@@ -385,17 +385,15 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
 constexpr int EXP_EPI_WARPS = 8;
 constexpr int EXP_THREADS = (EXP_EPI_WARPS + 3) * 32;
 
-// Shared memory: V hi / lo (128 rows: the MMA's M), then EBUF pipeline buffers, each with the y
-// tile of one 64-column block (bm rows x 128 B) followed by its B rows (one MN atom: rpad K rows
-// x 128 B).
+// Shared memory: EBUF pipeline buffers, each with the y tile of one 64-column block (bm rows x
+// 128 B) followed by its B rows (one MN atom: rpad K rows x 128 B). V (the MMA's A operand) lives in
+// tensor memory, which leaves the shared memory to the ring.
 struct ExpandSmem {
-  int nbuf, v_off, buf_off, buf_bytes, b_in_buf, bar_off, total;
+  int nbuf, buf_off, buf_bytes, b_in_buf, bar_off, total;
   // nbuf = 0: as many buffers as fit in `budget` bytes
   __host__ __device__ static ExpandSmem make(int rpad, int bm, int nbuf = 0, int budget = 227 * 1024) {
     ExpandSmem L;
-    const int katoms = (rpad + BK - 1) / BK;
-    L.v_off = 0;
-    L.buf_off = 2 * katoms * BM * 128;
+    L.buf_off = 0;
     L.b_in_buf = bm * 128;
     L.buf_bytes = (L.b_in_buf + rpad * 128 + 1023) & ~1023;
     const int fixed = 1024 + (2 * SCAN_CAP + 1) * 4 + 1024;
@@ -408,6 +406,8 @@ struct ExpandSmem {
 };
 
 constexpr int EBN = 64;  // expand: columns per pipeline block (MMA N)
+constexpr int kExpandVCol = 2 * EBN;      // first TMEM column of V
+constexpr int kExpandTmemCols = 256;      // 2 accumulators + V hi + V lo (rpad <= 128: 128 columns)
 
 template <int DT>
 __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_constant__ CUtensorMap tm_b,
@@ -417,7 +417,6 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
   uint8_t *smem = align1024(smem_raw);
   const ExpandSmem L = ExpandSmem::make(p.rpad, p.bm, p.stages);
   const int EBUF = L.nbuf;
-  const int katoms = (p.rpad + BK - 1) / BK;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);  // [EBUF] y tile + B rows landed
   uint64_t *empty = full + MAX_EBUF;      // [EBUF] the buffer's y tile has been stored (or written)
   uint64_t *accfull = empty + MAX_EBUF;   // [2] accumulator a holds a finished block
@@ -451,7 +450,9 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
     tc::tma_prefetch_desc(&tm_b);
     tc::tma_prefetch_desc(&tm_y);
   }
-  if (warp == 0) tc::tmem_alloc(tmem_slot, 2 * EBN);
+  // tensor memory: two EBN-column accumulators, then V hi (rpad / 2 columns: two 16-bit elements
+  // per column) and V lo; two CTAs per SM take all 512 columns
+  if (warp == 0) tc::tmem_alloc(tmem_slot, kExpandTmemCols);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -496,11 +497,12 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
   if (active && warp == EXP_EPI_WARPS && (p.paged || lane == 0))
     for (; issued < nblk && issued < EBUF; ++issued) issue(issued);
 
-  // V hi / lo in the K-major 128-byte-swizzle layout: epilogue thread m owns row m. fp16 rows
-  // are stored as v * 2^-vexp[m], with vexp[m] chosen so that the row's largest |v| stays below
-  // 2^14 (fp16 overflows at 65504, where bf16 and the fp32 v do not); the epilogue of row m
-  // multiplies its sums by 2^vexp[m]. The scaling is exact (a power of two); bf16 rows are not
-  // scaled.
+  // V hi / lo in tensor memory (the MMA's A operand, K-major): thread m of warps 0-3 writes row m
+  // (TMEM lane m), columns kExpandVCol + c hold elements 2c, 2c + 1 of V hi, and rpad / 2 columns
+  // further those of V lo. fp16 rows are stored as v * 2^-vexp[m], with vexp[m] chosen so that the
+  // row's largest |v| stays below 2^14 (fp16 overflows at 65504, where bf16 and the fp32 v do not);
+  // the epilogue of row m multiplies its sums by 2^vexp[m]. The scaling is exact (a power of two);
+  // bf16 rows are not scaled.
   int32_t *vexp = reinterpret_cast<int32_t *>(smem + L.bar_off + 512);  // [BM]
   if (active && warp < 4) {
     const int m = tid;
@@ -525,7 +527,7 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
     float rs = 1.f;  // 2^-vexp[m]
     if constexpr (DT == MLORA_FP16) {
       float amax = 0.f;
-      for (int c8 = 0; c8 < katoms * 8; ++c8) {
+      for (int c8 = 0; c8 < p.rpad / 8; ++c8) {
         float f[8];
         load8(c8, f);
 #pragma unroll
@@ -539,7 +541,8 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
     } else {
       vexp[m] = 0;
     }
-    for (int c8 = 0; c8 < katoms * 8; ++c8) {  // 16-byte chunks of 8 K elements
+    const uint32_t vrow_t = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kExpandVCol;
+    for (int c8 = 0; c8 < p.rpad / 8; ++c8) {  // 8 K elements = 4 TMEM columns
       float f[8], hi[8], lo[8];
       load8(c8, f);
       if constexpr (DT == MLORA_FP16) {
@@ -551,13 +554,12 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
 #pragma unroll
       for (int e = 0; e < 8; ++e) lo[e] = f[e] - hi[e];
       const uint4 l = pack8<DT>(lo);
-      const int atom = c8 >> 3, ch = c8 & 7;
-      const int off = atom * (BM * 128) + m * 128 + ((ch ^ (m & 7)) << 4);
-      *reinterpret_cast<uint4 *>(smem + L.v_off + off) = h;
-      *reinterpret_cast<uint4 *>(smem + L.v_off + katoms * BM * 128 + off) = l;
+      tc::tmem_st4(vrow_t + (uint32_t)(c8 * 4), h);
+      tc::tmem_st4(vrow_t + (uint32_t)(p.rpad / 2 + c8 * 4), l);
     }
-    tc::fence_proxy_async();
+    tc::tmem_st_wait();
   }
+  tc::tc_fence_before();
   __syncthreads();
 
   if (active && warp == EXP_EPI_WARPS) {
@@ -599,12 +601,11 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
         }
         tc::tc_fence_after();
         const int ksteps = p.rpad / 16;
-        for (int part = 0; part < 2; ++part) {  // V hi, then V lo
+        for (int part = 0; part < 2; ++part) {  // V hi, then V lo (from tensor memory)
           for (int kk = 0; kk < ksteps; ++kk) {
-            const uint8_t *va = smem + L.v_off + part * katoms * BM * 128 + (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-            const uint64_t da = tc::smem_desc_sw128(va, 16, 1024);
+            const uint32_t va = tmem + (uint32_t)(kExpandVCol + part * (p.rpad / 2) + kk * 8);  // 16 K elements
             const uint64_t db = tc::smem_desc_sw128(bs + kk * 16 * 128, 16, 1024);
-            tc::mma_f16(tmem + (uint32_t)(a * EBN), da, db, idesc, (part > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_f16_tmem_a(tmem + (uint32_t)(a * EBN), va, db, idesc, (part > 0 || kk > 0) ? 1u : 0u);
           }
         }
         tc::mma_commit(&accfull[a]);
@@ -686,7 +687,7 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
   if (active && flags[0] && tid == 0) report(p.status, MLORA_STATUS_TIMEOUT);
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 2 * EBN);
+  if (warp == 0) tc::tmem_dealloc(tmem, kExpandTmemCols);
 }
 
 // ------------------------------------------------------------------------------------------
