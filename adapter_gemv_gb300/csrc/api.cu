@@ -155,8 +155,8 @@ int run(int mode, int dtype, mlora::DecodeParams d, void *stream, bool pdl) {
 }
 
 // The tensor-core kernels for the long segments of one problem (prefill_tc.cu): segments of at
-// least kTcMinRows rows, in 128-row blocks (the last one masked). Marks the problem so that the
-// CUDA-core kernel launched after them takes only the shorter segments.
+// least tc_min_rows(nseg) rows, in blocks of at most 128 rows (the last one masked). Marks the
+// problem so that the CUDA-core kernel launched after them takes only the shorter segments.
 int run_tc(int mode, mlora::ProblemDev &q, const mlora_pool *pool, const int32_t *off, const int32_t *seg_slot,
            int32_t nseg, int32_t num_rows, int32_t *status, void *stream) {
   mlora::TcParams tp{};
@@ -176,6 +176,7 @@ int run_tc(int mode, mlora::ProblemDev &q, const mlora_pool *pool, const int32_t
   tp.y = q.y;
   tp.ldy = q.ldy;
   tp.status = status;
+  tp.tc_min = mlora::tc_min_rows(nseg);
   tp.paged = q.pool.kind == MLORA_POOL_PAGED ? 1 : 0;
   tp.page_elems = (int32_t)q.pool.page_elems;
   tp.a_ppv = q.pool.a_ppv;
@@ -195,13 +196,13 @@ int run_tc(int mode, mlora::ProblemDev &q, const mlora_pool *pool, const int32_t
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core expand launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }
-  q.tc_min = mlora::kTcMinRows;
+  q.tc_min = tp.tc_min;
   return MLORA_OK;
 }
 
 // SGMV over the problems of d: for each problem whose batch may hold long segments (a prefill
 // batch, or prefill and decode rows mixed), the tensor-core kernels take the segments of at least
-// kTcMinRows rows; then one CUDA-core launch takes every other segment of every problem.
+// tc_min_rows(nseg) rows; then one CUDA-core launch takes every other segment of every problem.
 int run_sgmv(int mode, mlora::DecodeParams &d, const mlora_pool *const *pools, void *stream, bool pdl) {
   bool any_tc = false;
   for (int q = 0; q < d.nprob; ++q) {

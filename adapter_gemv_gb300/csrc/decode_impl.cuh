@@ -440,6 +440,24 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   const ProblemDev &pr = p.prob[prob];
   const PoolDev &pl = pr.pool;
 
+  // After the tensor-core kernels the launch is sized for the worst case the host can see (every
+  // segment just short of tc_min rows): the tiles past the short segments' actual count leave
+  // before any setup (tile 0 always stays: it checks the offsets and reports them if malformed).
+  if (p.seg_off != nullptr && pr.tc_min > 0 && p.nseg <= SCAN_CAP && t > 0) {
+    int32_t *short_tiles = reinterpret_cast<int32_t *>(smem + 96);  // free bytes before gbuf
+    if (warp == 0) {
+      int32_t n = 0;
+      for (int q = lane; q < p.nseg; q += 32) {
+        const int32_t len = p.seg_off[q + 1] - p.seg_off[q];
+        if (len > 0 && len < pr.tc_min) n += (len + p.rt - 1) / p.rt;
+      }
+      n = (int32_t)__reduce_add_sync(0xffffffffu, (uint32_t)n);
+      if (lane == 0) *short_tiles = n;
+    }
+    __syncthreads();
+    if (t >= *short_tiles) return;  // uniform: the whole block, and every CTA of its cluster
+  }
+
   if (tid == 0) {
     mbar_init(xbar, 1);
     mbar_init(bbar, 1);

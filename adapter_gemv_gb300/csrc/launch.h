@@ -71,7 +71,15 @@ struct TcParams {
   const int32_t *a_tab, *b_tab;
 };
 
+// Segments of at least tc_min rows go to the tensor-core kernels, the shorter ones to the CUDA-core
+// kernel, whose launch is sized for the worst case the host can see: every segment just short of
+// tc_min rows. The host picks tc_min per call (tc_min_rows): kTcMinRows, lowered towards
+// kTcMinRowsLow so that this worst case stays near one CTA per SM -- in a prefill batch of a few long
+// prompts that launch is otherwise mostly empty tiles (8 prompts, 13B fused call: 18 us of a 115 us
+// call).
 constexpr int kTcMinRows = 32;
+constexpr int kTcMinRowsLow = 8;
+int tc_min_rows(int nseg);
 
 // Number of SMs of the current device (cached per device ordinal, safe from any host thread).
 int sm_count();

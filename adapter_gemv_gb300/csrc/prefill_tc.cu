@@ -1,10 +1,10 @@
 // prefill_tc.cu -- tensor-core path for long SGMV segments (prefill), sm_103a.
 //
-// A long segment that shares one adapter is a real dense contraction ("the segments are short
-// and fat, so the work is closer to a GEMM", "Multi-LoRA Serving, in depth", section "Two shapes:
-// SGMV for prefill, BGMV for decode"; Punica section 3.4, "Tensor Core usage"). Segments of at
-// least kTcMinRows rows run here in 128-row tiles, the last one masked; shorter segments run on
-// the CUDA-core kernels. bf16 and fp16 stacked pools; the MMAs are kind::f16 with both operands of
+// A long segment that shares one adapter is a real dense contraction: many rows against one
+// adapter's narrow matrices, a GEMM rather than a batch of GEMVs ("Multi-LoRA Serving, in depth",
+// section "Two shapes: SGMV for prefill, BGMV for decode"; Punica section 3.4, "Tensor Core
+// usage"). Segments of at least tc_min rows (the host's choice per call, 8 to 32) run here in
+// tiles of at most 128 rows, the last one masked; shorter segments run on the CUDA-core kernels. bf16 and fp16 stacked pools; the MMAs are kind::f16 with both operands of
 // the pool's type and fp32 accumulators.
 //
 //   shrink  V[128 x r] = X[128 x d_in] . A   : one CTA per (tile, K part); a cluster of K parts
@@ -733,8 +733,13 @@ cudaError_t set_smem(K kern, size_t smem) {
 
 }  // namespace
 
-// Segments of at least this many rows run on the tensor cores (last block masked).
-constexpr int TC_MIN_ROWS = kTcMinRows;
+// Rows from which a segment runs on the tensor cores: kTcMinRows, lowered for a batch of few
+// segments so that nseg * (tc_min - 1) -- the short-segment tiles the CUDA-core launch is sized
+// for -- stays near the SM count; at least kTcMinRowsLow.
+int tc_min_rows(int nseg) {
+  const int t = 1 + sm_count() / (nseg > 0 ? nseg : 1);
+  return t < kTcMinRowsLow ? kTcMinRowsLow : t > kTcMinRows ? kTcMinRows : t;
+}
 
 // The host does not see the segment lengths, only the batch's size: the tensor-core kernels are
 // launched for a batch with enough rows for long segments to be worth two extra launches (at
@@ -766,7 +771,6 @@ cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stre
   const PoolDev &pl = pr.pool;
   p.rpad = (pl.r_max + 15) & ~15;
   p.tmem_cols = p.rpad <= 32 ? 32 : p.rpad <= 64 ? 64 : 128;
-  p.tc_min = TC_MIN_ROWS;
   p.bm = tile_rows(p.M, p.nseg);
   p.tiles = p.M / p.bm + p.nseg;  // >= sum over long segments of ceil(len / bm)
   if (p.tiles <= 0) return cudaSuccess;
@@ -809,7 +813,6 @@ cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stre
 cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stream) {
   const PoolDev &pl = pr.pool;
   p.rpad = (pl.r_max + 15) & ~15;
-  p.tc_min = TC_MIN_ROWS;
   // Full 128-row tiles: the expand's cost per block is its y tile's pipeline pass, and tiles of
   // fewer rows measured slower (13B prefill, 7 expands: 689 us with 128 rows, 776 us with 88).
   p.bm = BM;
