@@ -200,18 +200,71 @@ int run_tc(int mode, mlora::ProblemDev &q, const mlora_pool *pool, const int32_t
   return MLORA_OK;
 }
 
+// A second stream, per host thread and device, for the CUDA-core launch of a call that also runs
+// tensor-core kernels. The two take disjoint rows (the short and the long segments), so they may
+// run at the same time: with a few long prompts mixed with decode rows the tensor-core kernels
+// fill only part of the SMs, and the CUDA-core kernel's rows would otherwise wait behind them.
+// Created on the thread's first such call whose stream is not being captured; until then (and
+// for lora_sgmv_noalloc, which creates nothing) the launches stay on the caller's stream.
+struct SideStream {
+  cudaStream_t stream;
+  cudaEvent_t forked, joined;  // caller's stream -> side stream, and back
+  bool ready, failed;
+};
+thread_local SideStream g_side[mlora::kMaxDevices];
+
+SideStream *side_stream(cudaStream_t caller) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= mlora::kMaxDevices) return nullptr;
+  SideStream &s = g_side[dev];
+  if (s.ready) return &s;
+  if (s.failed) return nullptr;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
+  if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess) {
+    s.failed = true;
+    return nullptr;
+  }
+  if (cudaEventCreateWithFlags(&s.forked, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&s.joined, cudaEventDisableTiming) != cudaSuccess) {
+    s.failed = true;
+    return nullptr;
+  }
+  s.ready = true;
+  return &s;
+}
+
 // SGMV over the problems of d: for each problem whose batch may hold long segments (a prefill
 // batch, or prefill and decode rows mixed), the tensor-core kernels take the segments of at least
-// tc_min_rows(nseg) rows; then one CUDA-core launch takes every other segment of every problem.
-int run_sgmv(int mode, mlora::DecodeParams &d, const mlora_pool *const *pools, void *stream, bool pdl) {
+// tc_min_rows(nseg) rows; one CUDA-core launch takes every other segment of every problem, on
+// the side stream when there is one (forked from the caller's stream before the tensor-core
+// launches, joined back after them).
+int run_sgmv(int mode, mlora::DecodeParams &d, const mlora_pool *const *pools, void *stream, bool pdl,
+             bool side_ok = true) {
   bool any_tc = false;
-  for (int q = 0; q < d.nprob; ++q) {
-    if (!mlora::tc_eligible(d.prob[q].pool, d.M, d.nseg)) continue;
-    TRY(run_tc(mode, d.prob[q], pools[q], d.seg_off, d.seg_slot, d.nseg, d.M, d.status, stream));
-    any_tc = true;
+  for (int q = 0; q < d.nprob && !any_tc; ++q) any_tc = mlora::tc_eligible(d.prob[q].pool, d.M, d.nseg);
+  if (!any_tc) return run(mode, pools[0]->dtype, d, stream, pdl);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  SideStream *side = side_ok ? side_stream(st) : nullptr;
+  if (side) {
+    cudaError_t e = cudaEventRecord(side->forked, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->forked, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "fork to the side stream");
   }
-  // after a tensor-core launch the decode kernel's dependency is that launch (no PDL needed)
-  return run(mode, pools[0]->dtype, d, stream, pdl && !any_tc);
+  int rc = MLORA_OK;
+  for (int q = 0; q < d.nprob && rc == MLORA_OK; ++q) {
+    if (!mlora::tc_eligible(d.prob[q].pool, d.M, d.nseg)) continue;
+    rc = run_tc(mode, d.prob[q], pools[q], d.seg_off, d.seg_slot, d.nseg, d.M, d.status, stream);
+  }
+  // after a tensor-core launch the CUDA-core kernel needs no early start (no PDL): on the caller's
+  // stream its dependency is that launch; on the side stream, the work before the call
+  if (rc == MLORA_OK) rc = run(mode, pools[0]->dtype, d, side ? side->stream : stream, false);
+  if (side) {  // joined even after an error: nothing is left on the side stream (nor in a capture)
+    cudaError_t e = cudaEventRecord(side->joined, side->stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, side->joined, 0);
+    if (e != cudaSuccess && rc == MLORA_OK) rc = cuda_fail(e, "join from the side stream");
+  }
+  return rc;
 }
 
 mlora::ProblemDev problem(const mlora_pool *pool, int32_t layer, const void *x, int64_t ldx, void *y, int64_t ldy,
@@ -337,7 +390,7 @@ int lora_sgmv_noalloc(void *y, int64_t ldy, const void *x, int64_t ldx, const ml
   mlora::DecodeParams d = base_params(seg_offsets, seg_slot, num_segments, nullptr, num_rows, dev_status);
   d.prob[0] = problem(pool, layer, x, ldx, y, ldy, v);
   d.nprob = 1;
-  return run_sgmv(mlora::MODE_FUSED, d, &pool, stream, g_pdl != 0);
+  return run_sgmv(mlora::MODE_FUSED, d, &pool, stream, g_pdl != 0, false);
 }
 
 int lora_bgmv_ex(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_pool *pool, const int32_t *row_slot,

@@ -165,6 +165,50 @@ def test_mixed_prefill_and_decode_batch(dev, form):
         check_op(op, batch, "sgmv", y, v if form == "two_phase" else None, what=f"mixed batch {form}")
 
 
+def test_mixed_batch_side_stream_and_graphs(dev):
+    """The CUDA-core launch of a mixed batch runs on a second stream, beside the tensor-core
+    kernels (forked from the caller's stream, joined back). A thread whose first such call is being
+    captured in a CUDA graph keeps every launch on the caller's stream; a thread that has its second
+    stream forks inside a capture too. Eager, captured-serial and captured-forked calls give the
+    same bits, and the oracle's results."""
+    import threading
+    pool, batch, x, y0 = mixed_batch(dev, torch.bfloat16, 23, 1024, 1032)
+    h = m.make_pool(pool)
+    M = batch.M
+
+    def call(y, v, st):
+        m.lora_sgmv(y, x, h, batch.seg_offsets, batch.seg_slot, 0, v, st)
+
+    def captured(out):
+        y, v = y0.clone(), new_v(M, 16, dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            call(y, v, st)
+        y.copy_(y0)
+        g.replay()
+        torch.cuda.synchronize()
+        out.append((y.clone(), st.item()))
+
+    fresh = []  # a new host thread: the first call is captured (no second stream yet)
+    t = threading.Thread(target=captured, args=(fresh,))
+    t.start()
+    t.join()
+    assert len(fresh) == 1, "the capture in a new thread failed"
+    y_e, v_e = y0.clone(), new_v(M, 16, dev)  # eager, forked
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    call(y_e, v_e, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    forked = []
+    captured(forked)  # this thread has its second stream now: the capture forks
+    for y, status in fresh + forked:
+        assert status == 0
+        assert torch.equal(y, y_e), "a captured call differs from the eager call"
+    check_op(W.Op("mixed", pool, 0, x, y0), batch, "sgmv", y_e, None, what="mixed batch, side stream")
+
+
 # Paged pools on the tensor cores (S-LoRA "Unified Paging", MBGMM-style prefill over the pages):
 # the A^T / B rows of a tile are gathered from their pages; pages as long as a vector, and pages
 # shorter than a vector (one H-vector per page: 13B MLP rows of 13824 span three 5120-element
