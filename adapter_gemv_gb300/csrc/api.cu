@@ -192,7 +192,7 @@ int run_tc(int mode, mlora::ProblemDev &q, const mlora_pool *pool, const int32_t
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }
   if (mode != mlora::MODE_SHRINK) {
-    const cudaError_t e = mlora::launch_tc_expand(q, tp, st);
+    const cudaError_t e = mlora::launch_tc_expand(q, tp, st, mode == mlora::MODE_FUSED);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core expand launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }

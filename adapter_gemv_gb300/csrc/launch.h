@@ -89,7 +89,9 @@ constexpr int kMaxDevices = 64;  // devices with a cached entry; others are quer
 // kernels for its long segments (decided on the host, which does not see the segment lengths).
 bool tc_eligible(const PoolDev &pool, int num_rows, int nseg);
 cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stream);
-cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stream);
+// after_shrink: launched right behind launch_tc_shrink of the same problem on the same stream
+// (a fused call); the expand then starts early and waits for the shrink before reading v.
+cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stream, bool after_shrink);
 
 // Device-side grouping of BGMV rows (bgmv_plan.cu): the rows in order of (rank descending, slot,
 // row) into perm / sslot [num_rows] each. At most kPlanMaxRows rows.

@@ -236,6 +236,8 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the expand of a fused call may start now: it reads v only after waiting for this grid
+  pdl_launch_dependents();
 
   resolve_tc_tile(p, t, ti, scan);
   int32_t *ptab = scan;  // paged: the scan area is free after the resolve
@@ -466,7 +468,6 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
     bad |= MLORA_STATUS_BAD_PAGE;
     active = false;
   }
-  if (blockIdx.x == 0 && tid == 0 && bad) report(p.status, bad);
   const int row0 = ti->row0, nr = ti->nr, s = ti->slot, rank = ti->rank;
   const float scale = ti->scale;
   const bool full_tile = nr == p.bm;  // a partial tile writes its rows with plain stores: the
@@ -496,6 +497,14 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
   };
   if (active && warp == EXP_EPI_WARPS && (p.paged || lane == 0))
     for (; issued < nblk && issued < EBUF; ++issued) issue(issued);
+
+  // Launched right behind the shrink of the same call (programmatic dependent launch), the kernel
+  // has so far read only what that shrink does not write: metadata, page tables, B rows and the
+  // y tiles (written, if at all, by work that completed before the shrink started). v and the
+  // status word wait for the shrink's grid. Every CTA waits, so this grid never completes before
+  // the shrink's.
+  pdl_wait();
+  if (blockIdx.x == 0 && tid == 0 && bad) report(p.status, bad);
 
   // V hi / lo in tensor memory (the MMA's A operand, K-major): thread m of warps 0-3 writes row m
   // (TMEM lane m), columns kExpandVCol + c hold elements 2c, 2c + 1 of V hi, and rpad / 2 columns
@@ -810,7 +819,7 @@ cudaError_t launch_tc_shrink(const ProblemDev &pr, TcParams p, cudaStream_t stre
   return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_a, p);
 }
 
-cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stream) {
+cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stream, bool after_shrink) {
   const PoolDev &pl = pr.pool;
   p.rpad = (pl.r_max + 15) & ~15;
   // Full 128-row tiles: the expand's cost per block is its y tile's pipeline pass, and tiles of
@@ -841,9 +850,19 @@ cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stre
   auto kern = pl.dtype == MLORA_BF16 ? tc_expand_kernel<MLORA_BF16> : tc_expand_kernel<MLORA_FP16>;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((p.nblk_total + p.nper - 1) / p.nper, p.tiles, 1);
-  kern<<<grid, EXP_THREADS, smem, stream>>>(tm_b, tm_y, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.nblk_total + p.nper - 1) / p.nper, p.tiles, 1);
+  cfg.blockDim = dim3(EXP_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  // right behind the tensor-core shrink of the same call: start early (programmatic dependent
+  // launch), the kernel waits for the shrink before it reads v
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_shrink ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, tm_b, tm_y, p);
 }
 
 }  // namespace mlora
