@@ -55,11 +55,21 @@ struct TcTile {
 // Tile t = the t-th block of p.bm rows, walking the segments in order: a segment of at least
 // p.tc_min rows contributes ceil(len / bm) blocks (the last one may be partial: nr < bm);
 // shorter segments belong to the CUDA-core kernels. Whole block participates; row metadata only.
+// A pool of at most blockDim.x slots has its rank and scale tables loaded at the start, beside the
+// offsets (one round trip to memory instead of two).
 __device__ void resolve_tc_tile(const TcParams &p, int t, TcTile *ti, int32_t *scan) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool cached = p.num_slots <= (int)blockDim.x;
+  int32_t my_rank = 0;
+  float my_scale = 0.f;
+  if (cached && tid < p.num_slots) {
+    my_rank = p.rank[tid];
+    my_scale = p.scale[tid];
+  }
   if (tid == 0) {
     ti->skip = 1;
     ti->bad = 0;
+    ti->slot = -2;
   }
   __syncthreads();
   int32_t carry = 0, found = 0, bad = 0;
@@ -101,6 +111,14 @@ __device__ void resolve_tc_tile(const TcParams &p, int t, TcTile *ti, int32_t *s
     }
     __syncthreads();
   }
+  if (cached) {  // the thread of the tile's slot hands over the rank and scale it loaded
+    const int s = ti->slot;
+    if (s >= 0 && s == tid) {
+      ti->rank = my_rank;
+      ti->scale = my_scale;
+    }
+    __syncthreads();
+  }
   if (tid == 0) {
     int32_t b = bad ? MLORA_STATUS_BAD_OFFSETS : 0;
     int skip = (!found || b) ? 1 : 0;
@@ -112,13 +130,13 @@ __device__ void resolve_tc_tile(const TcParams &p, int t, TcTile *ti, int32_t *s
         b = MLORA_STATUS_BAD_SLOT;
         skip = 1;
       } else {
-        const int r = p.rank[s];
+        const int r = cached ? ti->rank : p.rank[s];
         if (r < 1 || r > p.r_max) {
           b = MLORA_STATUS_BAD_RANK;
           skip = 1;
         } else {
           ti->rank = r;
-          ti->scale = p.scale[s];
+          ti->scale = cached ? ti->scale : p.scale[s];
         }
       }
     }
@@ -329,8 +347,12 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
   if (nkb > 0) ok = mbar_wait(accbar, 0) ? 1 : 0;
   const int timed_out = __syncthreads_or(!ok || flags[0]);
   tc::tc_fence_after();
-  float *red = reinterpret_cast<float *>(smem);  // the ring is idle now: [128][rpad] fp32 partials
+  // The ring is idle now. It holds the tile's v rows: [128][rpad] fp32 partials for the cluster
+  // sum, or (no K split) [128][rpad + 4] for the copy out, which writes whole rows of v with
+  // 16-byte stores (thread m writing its own row would scatter 4-byte stores over 128 rows).
+  float *red = reinterpret_cast<float *>(smem);
   const int m = warp * 32 + lane;
+  const int rs_ = ks == 1 ? p.rpad + 4 : p.rpad;  // row stride in red (floats)
   if (active && !timed_out) {
     for (int c16 = 0; c16 < p.rpad / 16; ++c16) {
       float vals[16];
@@ -340,17 +362,33 @@ __global__ void __launch_bounds__(NTHREADS) tc_shrink_kernel(const __grid_consta
 #pragma unroll
         for (int e = 0; e < 16; ++e) vals[e] = 0.f;
       }
-      if (ks == 1) {
-        if (m < nr) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int j = c16 * 16 + e;
-            if (j < rank) p.v[(int64_t)(row0 + m) * p.r_max + j] = vals[e];
+      for (int e4 = 0; e4 < 4; ++e4)
+        *reinterpret_cast<float4 *>(red + m * rs_ + c16 * 16 + e4 * 4) =
+            make_float4(vals[e4 * 4], vals[e4 * 4 + 1], vals[e4 * 4 + 2], vals[e4 * 4 + 3]);
+    }
+    if (ks == 1) {
+      __syncthreads();  // uniform: active and timed_out are the block's
+      const bool vec = (p.r_max & 3) == 0 && (reinterpret_cast<uintptr_t>(p.v) & 15) == 0;
+      if (vec) {
+        const int rq = (rank + 3) >> 2;  // 4-float groups per row
+        for (int e = tid; e < nr * rq; e += NTHREADS) {
+          const int row = e / rq, j = (e - row * rq) * 4;
+          float *dst = p.v + (int64_t)(row0 + row) * p.r_max + j;
+          const float4 val = *reinterpret_cast<const float4 *>(red + row * rs_ + j);
+          if (j + 4 <= rank) {
+            *reinterpret_cast<float4 *>(dst) = val;
+          } else {
+            dst[0] = val.x;
+            if (j + 1 < rank) dst[1] = val.y;
+            if (j + 2 < rank) dst[2] = val.z;
           }
         }
       } else {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) red[m * p.rpad + c16 * 16 + e] = vals[e];
+        for (int e = tid; e < nr * rank; e += NTHREADS) {
+          const int row = e / rank, j = e - row * rank;
+          p.v[(int64_t)(row0 + row) * p.r_max + j] = red[row * rs_ + j];
+        }
       }
     }
   }
@@ -412,7 +450,7 @@ constexpr int kExpandVCol = 2 * EBN;      // first TMEM column of V
 constexpr int kExpandTmemCols = 256;      // 2 accumulators + V hi + V lo (rpad <= 128: 128 columns)
 
 template <int DT>
-__global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_constant__ CUtensorMap tm_b,
+__global__ void __launch_bounds__(EXP_THREADS, 2) tc_expand_kernel(const __grid_constant__ CUtensorMap tm_b,
                                                                 const __grid_constant__ CUtensorMap tm_y,
                                                                 const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -515,32 +553,48 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
   int32_t *vexp = reinterpret_cast<int32_t *>(smem + L.bar_off + 512);  // [BM]
   if (active && warp < 4) {
     const int m = tid;
-    const float *vrow = p.v + (int64_t)(row0 + (m < nr ? m : 0)) * p.r_max;
+    const bool row_ok = m < nr;
+    const float *vrow = p.v + (int64_t)(row0 + (row_ok ? m : 0)) * p.r_max;
     const bool vec = ((p.r_max & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.v) & 15) == 0);
-    auto load8 = [&](int c8, float (&f)[8]) {  // 8 K elements of row m, zero past the rank and nr
-      if (m >= nr) {
+    const int nc = p.rpad / 8;  // 8-element chunks of a row (at most 16)
+    // Chunks g .. g + VG - 1 of row m (those below nc) into f, zero past the rank and for rows past
+    // nr. A group inside the v row takes 2 VG loads of 16 bytes, all issued before any is used (the
+    // row comes from L2: one round trip per group); otherwise single guarded floats. VG = 4 keeps
+    // the kernel within the registers of two CTAs per SM.
+    constexpr int VG = 4;
+    auto load_group = [&](int g, float (&f)[VG][8]) {
+      if (vec && (g + VG) * 8 <= p.r_max) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = 0.f;
-      } else if (vec && c8 * 8 + 8 <= rank) {
-        const float4 a = *reinterpret_cast<const float4 *>(vrow + c8 * 8);
-        const float4 b = *reinterpret_cast<const float4 *>(vrow + c8 * 8 + 4);
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+        for (int u = 0; u < VG; ++u) {
+          const float4 lo4 = *reinterpret_cast<const float4 *>(vrow + (g + u) * 8);
+          const float4 hi4 = *reinterpret_cast<const float4 *>(vrow + (g + u) * 8 + 4);
+          f[u][0] = lo4.x; f[u][1] = lo4.y; f[u][2] = lo4.z; f[u][3] = lo4.w;
+          f[u][4] = hi4.x; f[u][5] = hi4.y; f[u][6] = hi4.z; f[u][7] = hi4.w;
+        }
+#pragma unroll
+        for (int u = 0; u < VG; ++u)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[u][e] = (row_ok && (g + u) * 8 + e < rank) ? f[u][e] : 0.f;
       } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = c8 * 8 + e;
-          f[e] = (j < rank) ? vrow[j] : 0.f;
-        }
+        for (int u = 0; u < VG; ++u)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = (g + u) * 8 + e;
+            f[u][e] = (row_ok && g + u < nc && j < rank) ? vrow[j] : 0.f;
+          }
       }
     };
     float rs = 1.f;  // 2^-vexp[m]
     if constexpr (DT == MLORA_FP16) {
       float amax = 0.f;
-      for (int c8 = 0; c8 < p.rpad / 8; ++c8) {
-        float f[8];
-        load8(c8, f);
+      for (int g = 0; g < nc; g += VG) {
+        float f[VG][8];
+        load_group(g, f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+        for (int u = 0; u < VG; ++u)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[u][e]));
       }
       int e2 = 0;
       (void)frexpf(amax, &e2);  // amax = mant * 2^e2, mant in [0.5, 1); e2 <= 128
@@ -551,20 +605,26 @@ __global__ void __launch_bounds__(EXP_THREADS) tc_expand_kernel(const __grid_con
       vexp[m] = 0;
     }
     const uint32_t vrow_t = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kExpandVCol;
-    for (int c8 = 0; c8 < p.rpad / 8; ++c8) {  // 8 K elements = 4 TMEM columns
-      float f[8], hi[8], lo[8];
-      load8(c8, f);
-      if constexpr (DT == MLORA_FP16) {
+    for (int g = 0; g < nc; g += VG) {
+      float f[VG][8];
+      load_group(g, f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] *= rs;
+      for (int u = 0; u < VG; ++u) {
+        if (g + u < nc) {  // 8 K elements = 4 TMEM columns
+          float hi[8], lo[8];
+          if constexpr (DT == MLORA_FP16) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[u][e] *= rs;
+          }
+          const uint4 h = pack8<DT>(f[u]);
+          unpack8<DT>(h, hi);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) lo[e] = f[u][e] - hi[e];
+          const uint4 l = pack8<DT>(lo);
+          tc::tmem_st4(vrow_t + (uint32_t)((g + u) * 4), h);
+          tc::tmem_st4(vrow_t + (uint32_t)(p.rpad / 2 + (g + u) * 4), l);
+        }
       }
-      const uint4 h = pack8<DT>(f);
-      unpack8<DT>(h, hi);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) lo[e] = f[e] - hi[e];
-      const uint4 l = pack8<DT>(lo);
-      tc::tmem_st4(vrow_t + (uint32_t)(c8 * 4), h);
-      tc::tmem_st4(vrow_t + (uint32_t)(p.rpad / 2 + c8 * 4), l);
     }
     tc::tmem_st_wait();
   }
