@@ -59,7 +59,12 @@ struct TileInfo {
   int32_t skip;  // nonzero: nothing to do for this tile
   int32_t bad;   // status bits found while resolving
   int32_t pad;
+  // paged pools: the page-table rows of the tile's slot and layer (entry j * ppv + q = page of
+  // piece q of vector j), A and B: the copy in shared memory when it fits, else the pool's tables.
+  // Read from here at each use (kept out of the registers of the hot loops).
+  const int32_t *a_tr, *b_tr;
 };
+static_assert(sizeof(TileInfo) <= 56, "TileInfo sits in [64, 120) of shared memory");
 
 // Element k of row j of A^T (d_in elements) or of B (d_out elements) of slot s, layer `layer`.
 // A paged vector spans ppv consecutive page-table entries: element k sits in entry
@@ -74,23 +79,24 @@ __device__ __forceinline__ int page_of(const PoolDev &pl, int k) {
 }
 
 // Branch-free, so that a batch of such addresses issues its table loads together (for one-page
-// vectors q is 0).
-__device__ __forceinline__ const uint16_t *paged_elem(const PoolDev &pl, const int32_t *tab, int ppv, int64_t t,
-                                                      int k) {
+// vectors q is 0). `tr` is the page-table row block of the tile's slot and layer: entry
+// j * ppv + q holds the page of piece q of vector j (the tile's copy in shared memory, or the
+// pool's table in global memory).
+__device__ __forceinline__ const uint16_t *paged_elem(const PoolDev &pl, const int32_t *tr, int ppv, int j, int k) {
   const int q = page_of(pl, k);
-  return pl.pages + (int64_t)tab[t * ppv + q] * pl.page_elems + (k - q * (int)pl.page_elems);
+  return pl.pages + (int64_t)tr[j * ppv + q] * pl.page_elems + (k - q * (int)pl.page_elems);
 }
 
-__device__ __forceinline__ const uint16_t *a_elem(const PoolDev &pl, int s, int layer, int j, int k) {
-  const int64_t t = ((int64_t)s * pl.num_layers + layer) * pl.r_max + j;
-  if (pl.kind == MLORA_POOL_STACKED) return pl.a_t + t * pl.d_in + k;
-  return paged_elem(pl, pl.a_tab, pl.a_ppv, t, k);
+__device__ __forceinline__ const uint16_t *a_elem(const PoolDev &pl, int s, int layer, int j, int k,
+                                                  const int32_t *a_tr) {
+  if (pl.kind == MLORA_POOL_STACKED) return pl.a_t + (((int64_t)s * pl.num_layers + layer) * pl.r_max + j) * pl.d_in + k;
+  return paged_elem(pl, a_tr, pl.a_ppv, j, k);
 }
 
-__device__ __forceinline__ const uint16_t *b_elem(const PoolDev &pl, int s, int layer, int j, int n) {
-  const int64_t t = ((int64_t)s * pl.num_layers + layer) * pl.r_max + j;
-  if (pl.kind == MLORA_POOL_STACKED) return pl.b + t * pl.d_out + n;
-  return paged_elem(pl, pl.b_tab, pl.b_ppv, t, n);
+__device__ __forceinline__ const uint16_t *b_elem(const PoolDev &pl, int s, int layer, int j, int n,
+                                                  const int32_t *b_tr) {
+  if (pl.kind == MLORA_POOL_STACKED) return pl.b + (((int64_t)s * pl.num_layers + layer) * pl.r_max + j) * pl.d_out + n;
+  return paged_elem(pl, b_tr, pl.b_ppv, j, n);
 }
 
 // Element n of the B rows of one slot and layer, for a batch of rank rows: the slot/layer part of
@@ -102,11 +108,10 @@ struct BRows {
   int64_t stride;        // stacked: d_out; paged: page_elems
   int32_t ppv, off;      // paged: table entries per row, n's offset in its page
   bool paged;
-  __device__ __forceinline__ BRows(const PoolDev &pl, int s, int layer, int n) {
-    const int64_t t0 = ((int64_t)s * pl.num_layers + layer) * pl.r_max;
+  __device__ __forceinline__ BRows(const PoolDev &pl, int s, int layer, int n, const int32_t *b_tr) {
     paged = pl.kind != MLORA_POOL_STACKED;
     if (!paged) {
-      base = pl.b + t0 * pl.d_out + n;
+      base = pl.b + ((int64_t)s * pl.num_layers + layer) * pl.r_max * pl.d_out + n;
       stride = pl.d_out;
       tab = nullptr;
       ppv = off = 0;
@@ -115,7 +120,7 @@ struct BRows {
       base = pl.pages;
       stride = pl.page_elems;
       ppv = pl.b_ppv;
-      tab = pl.b_tab + t0 * pl.b_ppv + q;
+      tab = b_tr + q;
       off = n - q * (int)pl.page_elems;
     }
   }
@@ -127,17 +132,18 @@ struct BRows {
 // f(ptr, off, count) for each piece of elements [k0, k1) of a vector that lies in one page (the
 // whole range for a stacked pool or square pages); off is the piece's first element minus k0.
 template <bool IS_A, class F>
-__device__ __forceinline__ void vec_pieces(const PoolDev &pl, int s, int layer, int j, int k0, int k1, F f) {
+__device__ __forceinline__ void vec_pieces(const PoolDev &pl, int s, int layer, int j, int k0, int k1,
+                                           const int32_t *tr, F f) {
   const int ppv = IS_A ? pl.a_ppv : pl.b_ppv;
   if (pl.kind == MLORA_POOL_STACKED || ppv == 1) {
-    if (k1 > k0) f(IS_A ? a_elem(pl, s, layer, j, k0) : b_elem(pl, s, layer, j, k0), 0, k1 - k0);
+    if (k1 > k0) f(IS_A ? a_elem(pl, s, layer, j, k0, tr) : b_elem(pl, s, layer, j, k0, tr), 0, k1 - k0);
     return;
   }
   const int pe = (int)pl.page_elems;
 #pragma unroll 1
   for (int k = k0; k < k1;) {
     const int end = min(k1, (page_of(pl, k) + 1) * pe);
-    f(IS_A ? a_elem(pl, s, layer, j, k) : b_elem(pl, s, layer, j, k), k - k0, end - k);
+    f(IS_A ? a_elem(pl, s, layer, j, k, tr) : b_elem(pl, s, layer, j, k, tr), k - k0, end - k);
     k = end;
   }
 }
@@ -149,7 +155,7 @@ __device__ __forceinline__ void vec_pieces(const PoolDev &pl, int s, int layer, 
 // when it has at most RANK_CACHE slots) is in flight at once: one round trip to memory.
 template <int MODE>
 __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t, TileInfo *ti, int32_t *scan,
-                             int32_t *rank_c, float *scale_c) {
+                             int32_t *rank_c, float *scale_c, int32_t *ptab) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool cached = pr.pool.num_slots <= RANK_CACHE;
   const bool sgmv = p.seg_off != nullptr;
@@ -306,9 +312,11 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
           const int64_t t0 = ((int64_t)s * pl.num_layers + pr.layer) * pl.r_max;
           int32_t badp = 0;
           // every page of every vector j < rank this mode reads: entries [0, na) of the A table's
-          // rows, then [na, na + nb) of the B table's, four loads in flight per lane at a time
+          // rows, then [na, na + nb) of the B table's, four loads in flight per lane at a time;
+          // kept in shared memory (ptab, the same order) when they fit p.npt entries
           const int na = MODE != MODE_EXPAND ? rank * pl.a_ppv : 0;
           const int nt = na + (MODE != MODE_SHRINK ? rank * pl.b_ppv : 0);
+          const bool keep = nt <= p.npt;
           for (int e0 = lane; e0 < nt; e0 += 128) {
             int32_t pg[4];
 #pragma unroll
@@ -317,9 +325,17 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
               pg[u] = e >= nt ? 0 : e < na ? pl.a_tab[t0 * pl.a_ppv + e] : pl.b_tab[t0 * pl.b_ppv + (e - na)];
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) badp |= (pg[u] < 0 || pg[u] >= pl.num_pages);
+            for (int u = 0; u < 4; ++u) {
+              const int e = e0 + 32 * u;
+              badp |= (pg[u] < 0 || pg[u] >= pl.num_pages);
+              if (keep && e < nt) ptab[e] = pg[u];
+            }
           }
           if (__any_sync(0xffffffffu, badp)) bad = MLORA_STATUS_BAD_PAGE;
+          if (lane == 0) {
+            ti->a_tr = keep ? ptab : pl.a_tab + t0 * pl.a_ppv;
+            ti->b_tr = keep ? ptab + na : pl.b_tab + t0 * pl.b_ppv;
+          }
         }
       }
       __syncwarp();
@@ -339,7 +355,7 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
 
 // Shared-memory layout (dynamic):
 //   [0, 64)      mbarriers: xbar (exchange), bbar (B rows staged), ibar (x slice), ybar (y slice)
-//   [64, 96)     TileInfo
+//   [64, 120)    TileInfo; [120, 124) the short-tile count of a launch after tensor-core kernels
 //   gbuf         [cs][RT][r_alloc] floats: every CTA's partial v (cluster modes)
 //   vsm          [RT][r_alloc] floats: the summed v of the tile
 //   xs           [RT][max(kb, xw)] elements: the tile's x rows, one pass or the whole slice (shrink)
@@ -351,8 +367,8 @@ __device__ void resolve_tile(const DecodeParams &p, const ProblemDev &pr, int t,
 //   Sharing the region keeps a CTA that stages B small enough to sit on an SM beside a CTA of
 //   the neighbouring launch.
 struct Layout {
-  int gbuf, vsm, xs, ys, scan, rank_c, scale_c, bs, total;
-  __host__ __device__ static Layout make(int cs, int rt, int r_alloc, int kb, int nb_staged, int ny, int xw) {
+  int gbuf, vsm, xs, ys, scan, rank_c, scale_c, bs, ptab, total;
+  __host__ __device__ static Layout make(int cs, int rt, int r_alloc, int kb, int nb_staged, int ny, int xw, int npt) {
     Layout L;
     L.gbuf = 128;
     L.vsm = L.gbuf + cs * rt * r_alloc * 4;
@@ -364,7 +380,8 @@ struct Layout {
     const int resolve_end = L.scale_c + RANK_CACHE * 4;
     L.bs = L.scan;
     const int staged_end = L.bs + r_alloc * nb_staged * 2;
-    L.total = resolve_end > staged_end ? resolve_end : staged_end;
+    L.ptab = ((resolve_end > staged_end ? resolve_end : staged_end) + 15) & ~15;
+    L.total = L.ptab + npt * 4;
     return L;
   }
 };
@@ -415,7 +432,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   constexpr int KB = Pass<JPW>::KB;
   const int cs = p.csplit;  // CTAs per tile: the cluster (SHRINK, FUSED) or the N-split (EXPAND)
   const bool stage_b = p.nb > 0;  // B rows of the CTA's slice go to shared memory before the wait
-  const Layout L = Layout::make(MODE == MODE_EXPAND ? 1 : cs, RT, p.r_alloc, KB, p.nb, p.ny, p.xw);
+  const Layout L = Layout::make(MODE == MODE_EXPAND ? 1 : cs, RT, p.r_alloc, KB, p.nb, p.ny, p.xw, p.npt);
   uint64_t *xbar = reinterpret_cast<uint64_t *>(smem);
   uint64_t *bbar = xbar + 1;
   uint64_t *ibar = xbar + 2;
@@ -444,7 +461,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   // segment just short of tc_min rows): the tiles past the short segments' actual count leave
   // before any setup (tile 0 always stays: it checks the offsets and reports them if malformed).
   if (p.seg_off != nullptr && pr.tc_min > 0 && p.nseg <= SCAN_CAP && t > 0) {
-    int32_t *short_tiles = reinterpret_cast<int32_t *>(smem + 96);  // free bytes before gbuf
+    int32_t *short_tiles = reinterpret_cast<int32_t *>(smem + 120);  // free bytes before gbuf
     if (warp == 0) {
       int32_t n = 0;
       for (int q = lane; q < p.nseg; q += 32) {
@@ -469,10 +486,12 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
   if (clustered) cluster_arrive_relaxed();  // peers may push into our gbuf once everyone arrived
   pdl_launch_dependents();                  // the next kernel may start; it waits for us before reading our outputs
 
-  resolve_tile<MODE>(p, pr, t, ti, scan, rank_c, scale_c);
+  int32_t *ptab = reinterpret_cast<int32_t *>(smem + L.ptab);
+  resolve_tile<MODE>(p, pr, t, ti, scan, rank_c, scale_c, ptab);
   const bool active = !ti->skip;  // uniform across the block and across the cluster
   const int row0 = ti->row0, nr = ti->nr, s = ti->slot, rank = ti->rank;
   const float scale = ti->scale;
+
 
   // This CTA's slices of d_in and d_out.
   const int kchunk = ((pl.d_in + cs - 1) / cs + 7) & ~7;
@@ -536,7 +555,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
     }
     if (do_shrink && k_end - k_begin > kbn)
       for (int j = lane; j < rank; j += 32)
-        vec_pieces<true>(pl, s, pr.layer, j, k_begin + kbn, k_end,
+        vec_pieces<true>(pl, s, pr.layer, j, k_begin + kbn, k_end, ti->a_tr,
                          [](const uint16_t *src, int, int n) { prefetch_l2(src, (uint32_t)n * 2); });
     if (clustered && lane == 0) mbar_arrive_expect_tx(xbar, (uint32_t)(cs * nr * rank * 4));
   }
@@ -552,14 +571,14 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       const int j = warp + jj * NWARPS;
       // the vector's start when it lies in one page (stacked pool, square pages): one table read
       // per rank row; else each chunk finds its page
-      const uint16_t *base = (j < rank && one_piece_a) ? a_elem(pl, s, pr.layer, j, 0) : nullptr;
+      const uint16_t *base = (j < rank && one_piece_a) ? a_elem(pl, s, pr.layer, j, 0, ti->a_tr) : nullptr;
 #pragma unroll
       for (int u = 0; u < UKN; ++u) {
         const int c8 = lane + 32 * u, i = jj * UKN + u;
         const int k = kb0 + c8 * 8;
         // zero outside the slice and the rank: the one-row loop below then needs no guards
         a[i / UK][i % UK] = (j < rank && c8 < n8)
-                                ? ldg_stream(one_piece_a ? base + k : a_elem(pl, s, pr.layer, j, k), evict_first)
+                                ? ldg_stream(one_piece_a ? base + k : a_elem(pl, s, pr.layer, j, k, ti->a_tr), evict_first)
                                 : make_uint4(0u, 0u, 0u, 0u);
       }
     }
@@ -570,14 +589,14 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
         if (lane == 0) mbar_arrive_expect_tx(bbar, (uint32_t)(rank * (n_end - n_begin) * 2));
         __syncwarp();
         for (int j = lane; j < rank; j += 32)
-          vec_pieces<false>(pl, s, pr.layer, j, n_begin, n_end, [&](const uint16_t *src, int off, int n) {
+          vec_pieces<false>(pl, s, pr.layer, j, n_begin, n_end, ti->b_tr, [&](const uint16_t *src, int off, int n) {
             bulk_g2s_hint(bs + j * p.nb + off, src, (uint32_t)n * 2, bbar, evict_first);
           });
       } else if (!(x_bulk && RT == 1 && k_end - k_begin > kbn)) {
         // (a tile that loops over several passes of A prefetches its B rows at its last pass:
         // issued now, they would queue ahead of the later passes' A rows)
         for (int j = lane; j < rank; j += 32)
-          vec_pieces<false>(pl, s, pr.layer, j, n_begin, n_end,
+          vec_pieces<false>(pl, s, pr.layer, j, n_begin, n_end, ti->b_tr,
                             [](const uint16_t *src, int, int n) { prefetch_l2(src, (uint32_t)n * 2); });
       }
   }
@@ -661,7 +680,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
           // prefetched them before the wait)
           if (pass > 0 && !b_staged && do_expand && n_end > n_begin && (pass + 1) * KBN >= k_end - k_begin)
             for (int j = tid; j < rank; j += NTHREADS)
-              vec_pieces<false>(pl, s, pr.layer, j, n_begin, n_end,
+              vec_pieces<false>(pl, s, pr.layer, j, n_begin, n_end, ti->b_tr,
                                 [](const uint16_t *src, int, int n) { prefetch_l2(src, (uint32_t)n * 2); });
 #pragma unroll
           for (int u = 0; u < UKN; ++u) {
@@ -807,7 +826,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       for (int j = 0; j < RV; ++j) vr[j] = (VREG && j < rank) ? vsm[j] : 0.f;
       for (int c8 = tid; c8 < n8; c8 += NTHREADS) {
         const int n0 = n_begin + c8 * 8;
-        const BRows brow(pl, s, pr.layer, n0);
+        const BRows brow(pl, s, pr.layer, n0, ti->b_tr);
         float2 ev[4], od[4];  // even / odd rank rows
 #pragma unroll
         for (int e = 0; e < 4; ++e) ev[e] = od[e] = make_float2(0.f, 0.f);
@@ -904,7 +923,7 @@ __global__ void __launch_bounds__(NTHREADS) decode_kernel(const __grid_constant_
       // broadcast read of shared memory) in paired fp32 FMAs.
       for (int c8 = tid; c8 < n8; c8 += NTHREADS) {
         const int n0 = n_begin + c8 * 8;
-        const BRows brow(pl, s, pr.layer, n0);
+        const BRows brow(pl, s, pr.layer, n0, ti->b_tr);
         float2 acc2[RT][4];
 #pragma unroll
         for (int i = 0; i < RT; ++i)

@@ -119,14 +119,26 @@ cudaError_t launch_decode(int mode, int dtype, DecodeParams p, cudaStream_t stre
     const int npass = (kchunk + kb - 1) / kb;
     p.xw = (mode != MODE_EXPAND && p.rt == 1 && npass > 1 && npass * kb * 2 <= 32 * 1024) ? npass * kb : 0;
   }
+  // Paged pools: the resolve reads every page id of the tile's vectors (to check them); they stay
+  // in shared memory for the address of every later load when they fit 8 KB (else the loads
+  // read the table in global memory, one dependent round trip each time).
+  p.npt = 0;
+  for (int q = 0; q < p.nprob; ++q) {
+    const PoolDev &pl = p.prob[q].pool;
+    if (pl.kind == MLORA_POOL_PAGED) {
+      const int need = pl.r_max * (pl.a_ppv + pl.b_ppv);
+      p.npt = p.npt > need ? p.npt : need;
+    }
+  }
+  if (p.npt > 2048) p.npt = 0;
   // The tile's y rows also go to shared memory, if the CTA stays small enough to share an SM
   // with another.
   const int lcs = (mode == MODE_EXPAND) ? 1 : cs;
   p.ny = 0;
   if (mode != MODE_SHRINK && p.rt * nchunk * 2 <= y_cap &&
-      Layout::make(lcs, p.rt, r_alloc, kb, p.nb, nchunk, p.xw).total <= y_total_cap)
+      Layout::make(lcs, p.rt, r_alloc, kb, p.nb, nchunk, p.xw, p.npt).total <= y_total_cap)
     p.ny = nchunk;
-  const Layout L = Layout::make(lcs, p.rt, r_alloc, kb, p.nb, p.ny, p.xw);
+  const Layout L = Layout::make(lcs, p.rt, r_alloc, kb, p.nb, p.ny, p.xw, p.npt);
   if (L.total > 227 * 1024) return cudaErrorInvalidConfiguration;
 
   const int64_t grid = units * cs;

@@ -45,6 +45,7 @@ struct DecodeParams {
   int32_t *status;
   uint64_t wait_ns;  // limit of the kernel's waits (0 = the default, kWaitLimitNs)
   // chosen by the launcher
+  int32_t npt;  // paged pools: page-table entries of a tile kept in shared memory (0: none)
   int32_t rt, tiles, csplit, kb, nb, ny, xw, r_alloc;  // nb: staged B columns; ny: y slice staged;
                                                       // xw: x row width staged (whole d_in slice), 0 = one pass
 };
