@@ -663,18 +663,20 @@ def run_reference(args):
 REFERENCE_BUDGET_S = 120.0
 
 
-NCU_TARGETS = ("decode7b", "decode7b-2layers", "q_proj", "prefill13b-q", "paged70b")
+NCU_TARGETS = ("decode7b", "decode7b-2layers", "decode7b-identical-2layers", "q_proj", "prefill13b-q", "paged70b")
 
 
 def run_ncu_target(name: str, reps: int):
     """Run one workload `reps` times with no timing, as a target for ncu (nothing is printed but
     'ok'). decode7b-2layers is the decode step with 2 layers: the same launches per layer, a
-    smaller footprint for multi-pass captures."""
+    smaller footprint for multi-pass captures; decode7b-identical-2layers the same with every row
+    on one adapter."""
     import adapter_gemv_gb300 as m
     from adapter_gemv_gb300.plan import StepPlan
     dev = torch.device("cuda", 0)
     if name.startswith("decode7b"):
-        w = W.sgmv_decode_7b(device=dev, num_layers=2 if name.endswith("2layers") else 32)
+        w = W.sgmv_decode_7b(device=dev, num_layers=2 if name.endswith("2layers") else 32,
+                             dist="identical" if "identical" in name else "distinct")
         plan = StepPlan(w.ops, w.batch)
         for _ in range(reps):
             plan()

@@ -67,19 +67,25 @@ def test_decode_step_7b_as_benched(dev, dist):
             check_op(op, w.batch, "sgmv", op.y, y_before=before[id(op)], what=f"{dist} {op.name} L{op.layer}")
 
 
-def ragged_rank16_step(dev, dtype, seed):
-    """Chained one-row problems whose pools have r_max 16 (the kernel that stages A in shared
-    memory): ranks 4/8/13/16 (padding rows hold NaN), d_in slices that end inside a pass of A
-    (2056, 11008), a d_out that is not a multiple of the split (1000), two rows without adapter."""
+def ragged_rank16_step(dev, dtype, seed, page_elems=None):
+    """Chained one-row problems whose pools have r_max 16: ranks 4/8/13/16 (padding rows hold NaN),
+    d_in slices that end inside a pass of A (2056, 11008), a d_out that is not a multiple of the
+    split (1000), a B much larger than A (up), two rows without adapter. page_elems: paged pools
+    with pages of that many elements (0: one page per vector), else stacked pools."""
     g = W.generator(seed, dev)
     rng = np.random.default_rng(seed)
-    projs = [W.Projection("q", 4096, 4096), W.Projection("k", 4096, 1024), W.Projection("o", 2056, 1000),
-             W.Projection("down", 11008, 4096)]
+    projs = [W.Projection("q", 4096, 4096), W.Projection("k", 4096, 1024), W.Projection("up", 4096, 11008),
+             W.Projection("o", 2056, 1000), W.Projection("down", 11008, 4096)]
     num_slots, M = 24, 20
     ranks = rng.choice(np.array([4, 8, 13, 16], np.int32), size=num_slots)
     ranks[:4] = [4, 8, 13, 16]
-    pools = {p.name: W.stacked_pool(num_slots=num_slots, num_layers=2, r_max=16, d_in=p.d_in, d_out=p.d_out,
-                                    dtype=dtype, gen=g, device=dev, ranks=ranks) for p in projs}
+    if page_elems is None:
+        pools = {p.name: W.stacked_pool(num_slots=num_slots, num_layers=2, r_max=16, d_in=p.d_in, d_out=p.d_out,
+                                        dtype=dtype, gen=g, device=dev, ranks=ranks) for p in projs}
+    else:
+        pools = {p.name: W.paged_pool(num_slots=num_slots, num_layers=2, r_max=16, d_in=p.d_in, d_out=p.d_out,
+                                      dtype=dtype, gen=g, device=dev, rng=rng, ranks=ranks,
+                                      page_elems=page_elems or None) for p in projs}
     slots = np.r_[[-1, -1], rng.permutation(num_slots)[:M - 2]].astype(np.int32)
     slots.sort(kind="stable")
     batch = W.batch_from_slots(slots, sgmv=True).to(dev)
@@ -89,16 +95,17 @@ def ragged_rank16_step(dev, dtype, seed):
     ops = []
     for layer in (0, 1):
         for p in projs:
-            x = x_qk if p.name in ("q", "k") else x_o if p.name == "o" else x_down
+            x = x_qk if p.name in ("q", "k", "up") else x_o if p.name == "o" else x_down
             ops.append(W.Op(p.name, pools[p.name], layer, x, W.uniform((M, p.d_out), -1, 1, dtype, g, dev)))
     return batch, ops
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
-def test_chained_rank16_step_ragged(dev, dtype):
+@pytest.mark.parametrize("dtype,page_elems", [(torch.bfloat16, None), (torch.float16, None),
+                                              (torch.bfloat16, 0), (torch.float16, 4096)])
+def test_chained_rank16_step_ragged(dev, dtype, page_elems):
     """A step plan (programmatic dependent launch) over ragged rank <= 16 problems: every op on
     every row against the oracle; rows without adapter keep their bits."""
-    batch, ops = ragged_rank16_step(dev, dtype, seed=11)
+    batch, ops = ragged_rank16_step(dev, dtype, seed=11, page_elems=page_elems)
     st = status_of(dev)
     before = {id(op): bits(op.y) for op in ops}
     plan = StepPlan(ops, batch, st)

@@ -282,3 +282,54 @@ def test_exact_rank1_closed_form(dev):
             continue
         want = scale[s] * d_in * xs[i] * a_value(s, 0) * np.array([b_value(s, 0, n) for n in range(d_out)])
         assert np.array_equal(got[i], want), f"row {i}: closed form differs"
+
+
+# Chained one-row calls (programmatic dependent launch), bit for bit: projections whose d_in slice
+# spans several passes of A and projections whose B is much larger than their A, on stacked pools
+# and on paged pools with one page per vector or pages shorter than the vectors.
+# dtype, paged, d_in, d_out, M, ranks, page_elems (None: one page per vector)
+CHAINED_CASES = [
+    (torch.bfloat16, False, 11008, 4096, 20, [16, 1, 7, 16, 3, 12], None),
+    (torch.float16, True, 11008, 4096, 20, [5, 16, 1, 9, 16, 2], None),
+    (torch.bfloat16, True, 11008, 4096, 24, [16, 4, 13, 16], 1536),
+    (torch.bfloat16, False, 4096, 11008, 32, [16, 1, 7, 16, 3, 12], None),
+    (torch.float16, True, 4096, 11008, 32, [16, 2, 9, 16, 8], 4096),
+]
+
+
+@pytest.mark.parametrize("case", CHAINED_CASES, ids=lambda c: f"{'bf16' if c[0] == torch.bfloat16 else 'fp16'}-"
+                         f"{'paged' if c[1] else 'stacked'}-{c[2]}x{c[3]}-M{c[4]}" + (f"-pages{c[6]}" if c[6] else ""))
+def test_exact_routing_chained_calls(dev, case):
+    dtype, paged, d_in, d_out, M, ranks, page_elems = case
+    rng = np.random.default_rng(zlib.crc32(repr(case[1:]).encode()))
+    pool = exact_pool(dev, dtype, num_slots=len(ranks), num_layers=2, r_max=16, d_in=d_in, d_out=d_out, ranks=ranks,
+                      paged=paged, rng=rng, page_elems=page_elems)
+    h = m.make_pool(pool)
+    layer = 1
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    off = np.arange(M + 1, dtype=np.int32)
+    seg_slot = rng.integers(-1, len(ranks), M).astype(np.int32)
+    x, y0 = exact_rows(dev, dtype, M, d_in, d_out, seg_slot)
+    offd, ssd = torch.from_numpy(off).to(dev), torch.from_numpy(seg_slot).to(dev)
+    v = torch.empty((M, 16), dtype=torch.float32, device=dev)
+    ys = [y0.clone() for _ in range(3)]
+    yg = [y0.clone() for _ in range(2)]
+    perm = rng.permutation(M)
+    rs_b = seg_slot[perm].astype(np.int32)
+    xb, yb0 = exact_rows(dev, dtype, M, d_in, d_out, rs_b)
+    yb = yb0.clone()
+    prev = m.lora_set_programmatic_launch(True)
+    try:
+        for q in range(3):  # chained: every call after the first waits on the previous one
+            m.lora_sgmv(ys[q], x, h, offd, ssd, layer, v, st)
+        m.lora_sgmv_grouped([(yg[q], x, h, layer, torch.empty_like(v)) for q in range(2)], offd, ssd, st)
+        m.lora_bgmv(yb, xb, h, torch.from_numpy(rs_b).to(dev), layer, v, st)
+    finally:
+        m.lora_set_programmatic_launch(prev)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for q in range(3):
+        check_exact(pool, layer, x, y0, ys[q], "sgmv", (off, seg_slot), None, f"chained sgmv {q}")
+    for q in range(2):
+        check_exact(pool, layer, x, y0, yg[q], "sgmv", (off, seg_slot), None, f"chained grouped problem {q}")
+    check_exact(pool, layer, xb, yb0, yb, "bgmv", rs_b, None, "chained bgmv")
