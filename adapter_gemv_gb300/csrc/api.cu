@@ -418,6 +418,14 @@ int lora_bgmv_ex(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_p
                                                   static_cast<cudaStream_t>(stream), pdl);
     if (e != cudaSuccess) return cuda_fail(e, "row grouping launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (mlora::stream_eligible(d.prob[0].pool, num_rows)) {
+      // heterogeneous ranks: one CTA per row, streaming its adapter rows (reads the order: no early start)
+      const cudaError_t es = mlora::launch_bgmv_stream(d.prob[0], perm, sslot, num_rows, dev_status, g_wait_limit_ns,
+                                                       static_cast<cudaStream_t>(stream));
+      if (es != cudaSuccess) return cuda_fail(es, "streaming BGMV launch");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+      return MLORA_OK;
+    }
     d.perm = perm;
     d.sslot = sslot;
     return run(mlora::MODE_FUSED, pool->dtype, d, stream, false);  // reads the order: no early start

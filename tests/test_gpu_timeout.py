@@ -101,3 +101,48 @@ def test_status_bit_survives_a_clear_just_before_a_programmatic_call(dev):
             assert st.item() == m.STATUS_BAD_SLOT
     finally:
         m.lora_set_programmatic_launch(prev)
+
+
+def test_short_wait_limit_streaming_bgmv(dev):
+    """The same for grouped BGMV rows of a heterogeneous-rank paged pool, which a cluster of CTAs
+    per row streams through shared-memory rings: producer and consumer warps give up on their
+    waits, the cluster's partial-sum exchange gives up too, the producers wait for the copies they
+    issued, and no element of y is wrong."""
+    g = W.generator(21, dev)
+    rng = np.random.default_rng(21)
+    ranks = np.array([8, 32, 16, 32, 8, 24], np.int32)
+    d_in, d_out = 8192, 4160  # a full-rank row is 786 KB: two CTAs per row
+    pool = W.paged_pool(num_slots=6, num_layers=1, r_max=32, d_in=d_in, d_out=d_out, dtype=torch.bfloat16, gen=g,
+                        device=dev, rng=rng, ranks=ranks, page_elems=1024)
+    M = 40
+    slots = rng.integers(-1, 6, M).astype(np.int32)
+    batch = W.batch_from_slots(slots, sgmv=False).to(dev)
+    x = W.normal((M, d_in), 1.0, torch.bfloat16, g, dev)
+    y0 = W.uniform((M, d_out), -1, 1, torch.bfloat16, g, dev)
+    op = W.Op("up", pool, 0, x, y0)
+    want, _, st_o = oracle_op(op, batch, "bgmv")
+    assert st_o == 0
+    dt = odt(pool.dtype)
+    before = bits(y0)
+    h = m.make_pool(pool)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    v = torch.empty((M, 32), dtype=torch.float32, device=dev)
+    m.lora_test_set_wait_limit_ns(2)
+    try:
+        for _ in range(3):
+            y = y0.clone()
+            m.lora_bgmv_ex(y, x, h, batch.row_slot, 0, v, m.LAUNCH_GROUP_ROWS, st)
+            torch.cuda.synchronize()
+            ok = untouched_or_correct(bits(y), before, want, dt)
+            assert ok.all(), f"{(~ok).sum()} elements neither untouched nor correct after a timed-out call"
+    finally:
+        m.lora_test_set_wait_limit_ns(0)
+    assert st.item() & m.STATUS_TIMEOUT, "no wait gave up with a limit of 2 ns"
+    assert st.item() & ~m.STATUS_TIMEOUT == 0
+    st.zero_()
+    y = y0.clone()
+    m.lora_bgmv_ex(y, x, h, batch.row_slot, 0, v, m.LAUNCH_GROUP_ROWS, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    gv, wv = oracle.decode(bits(y), dt), oracle.decode(want, dt)
+    assert np.all(np.abs(gv - wv) <= TOL * (1.0 + np.abs(wv)))
