@@ -414,14 +414,18 @@ int lora_bgmv_ex(void *y, int64_t ldy, const void *x, int64_t ldx, const mlora_p
   if (want && num_rows <= mlora::kPlanMaxRows && pool->r_max >= 2) {
     int32_t *perm = reinterpret_cast<int32_t *>(v_scratch);
     int32_t *sslot = perm + num_rows;
-    const cudaError_t e = mlora::launch_bgmv_plan(row_slot, num_rows, d.prob[0].pool, perm, sslot,
-                                                  static_cast<cudaStream_t>(stream), pdl);
+    // heterogeneous ranks: the grouped order is cut into segments of rows that share a slot
+    // (after perm and sslot in v_scratch: num_rows + 1 more int32), which the streaming kernel
+    // takes a cluster of CTAs at a time
+    const bool stream_rows = mlora::stream_eligible(d.prob[0].pool, num_rows);
+    int32_t *segs = stream_rows ? sslot + num_rows : nullptr;
+    const cudaError_t e = mlora::launch_bgmv_plan(row_slot, num_rows, d.prob[0].pool, perm, sslot, segs,
+                                                  mlora::kStreamSegRows, static_cast<cudaStream_t>(stream), pdl);
     if (e != cudaSuccess) return cuda_fail(e, "row grouping launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    if (mlora::stream_eligible(d.prob[0].pool, num_rows)) {
-      // heterogeneous ranks: one CTA per row, streaming its adapter rows (reads the order: no early start)
-      const cudaError_t es = mlora::launch_bgmv_stream(d.prob[0], perm, sslot, num_rows, dev_status, g_wait_limit_ns,
-                                                       static_cast<cudaStream_t>(stream));
+    if (stream_rows) {  // reads the order: no early start
+      const cudaError_t es = mlora::launch_bgmv_stream(d.prob[0], perm, sslot, segs, num_rows, dev_status,
+                                                       g_wait_limit_ns, static_cast<cudaStream_t>(stream));
       if (es != cudaSuccess) return cuda_fail(es, "streaming BGMV launch");
       g_launches.fetch_add(1, std::memory_order_relaxed);
       return MLORA_OK;

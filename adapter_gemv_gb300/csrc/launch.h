@@ -96,27 +96,32 @@ cudaError_t launch_tc_expand(const ProblemDev &pr, TcParams p, cudaStream_t stre
 
 // Device-side grouping of BGMV rows (bgmv_plan.cu): the rows in order of (rank descending, slot,
 // row) into perm / sslot [num_rows] each. At most kPlanMaxRows rows.
+// With segs != nullptr the order is also cut into segments of at most seg_rows rows that share a
+// slot: segs[0] = the count, segs[1 + k] = segment k's first position (M + 1 int32 at most).
 constexpr int kPlanMaxRows = 4096;
 cudaError_t launch_bgmv_plan(const int32_t *row_slot, int32_t M, const PoolDev &pool, int32_t *perm, int32_t *sslot,
-                             cudaStream_t stream, bool pdl);
+                             int32_t *segs, int32_t seg_rows, cudaStream_t stream, bool pdl);
 
-// BGMV rows of a heterogeneous-rank pool, in the grouped order, a cluster of CTAs per row streaming
-// its A^T and B rank-rows through shared-memory rings (bgmv_stream.cu).
+// BGMV rows of a heterogeneous-rank pool, in the grouped order cut into segments of rows that share
+// a slot: a cluster of CTAs per segment streams the adapter's A^T and B rank-rows through
+// shared-memory rings (bgmv_stream.cu).
+constexpr int kStreamSegRows = 4;  // rows per segment at most
 struct StreamParams {
   ProblemDev pr;
   const int32_t *perm, *sslot;  // the grouped order (bgmv_plan.cu)
+  const int32_t *segs;          // [0]: segment count, [1 + k]: first position of segment k
   int32_t M;
   int32_t *status;
   uint64_t wait_ns;
-  int32_t cs, kc, nc;          // CTAs per row (a cluster), each CTA's slice of d_in and of d_out
-  int32_t kpad, npad, stages;  // x / y slice buffer widths (elements), ring stages
-  int32_t ptn;                 // paged pools: page-table entries of one row (r_max (a_ppv + b_ppv))
+  int32_t cs, kc, nc;    // CTAs per segment (a cluster), each CTA's slice of d_in and of d_out
+  int32_t kpad, stages;  // x slice buffer width (elements), ring stages
+  int32_t ptn;           // paged pools: page-table entries of one slot (r_max (a_ppv + b_ppv))
 };
 // Whether lora_bgmv's grouped rows on this pool take the streaming kernel (r_max of 32 to 128 and
 // the buffers fit in shared memory).
 bool stream_eligible(const PoolDev &pool, int num_rows);
-cudaError_t launch_bgmv_stream(const ProblemDev &pr, const int32_t *perm, const int32_t *sslot, int32_t M,
-                               int32_t *status, uint64_t wait_ns, cudaStream_t stream);
+cudaError_t launch_bgmv_stream(const ProblemDev &pr, const int32_t *perm, const int32_t *sslot, const int32_t *segs,
+                               int32_t M, int32_t *status, uint64_t wait_ns, cudaStream_t stream);
 
 // CUDA-core path for decode-sized tiles (decode_launch.cu chooses the split and the stages;
 // decode_{shrink,expand,fused}.cu hold the kernels). force_csplit > 0 overrides the split.

@@ -175,11 +175,12 @@ MLORA_API int lora_bgmv(void *y, int64_t ldy, const void *x, int64_t ldx, const 
  * rows in that order. Rows of one adapter run side by side, so the adapter comes from HBM once;
  * the heaviest rows start first. The caller's row order, x and y are unchanged; the order is
  * kept in v_scratch (2 x num_rows int32). On pools of r_max 32 to 128 (S-LoRA section 3,
- * "Heterogeneous Batching Kernels": adapters of many ranks in one pool) and batches of up to
- * four rows per SM, the grouped rows go to a streaming kernel instead: a cluster of CTAs per row
- * streams the row's A^T and B rank-rows through shared-memory rings, rows in snake order over
- * the clusters, largest first. lora_bgmv groups batches of at least 128 rows (up to 4096 rows,
- * r_max >= 2); the flags override that:
+ * "Heterogeneous Batching Kernels": adapters of many ranks in one pool) the grouped order is
+ * also cut into segments of up to 4 rows that share a slot (num_rows + 1 more int32 of
+ * v_scratch), and a streaming kernel takes over: a cluster of CTAs per segment streams the
+ * adapter's A^T and B rank-rows through shared-memory rings once for the segment's rows,
+ * segments in snake order over the clusters, largest first. lora_bgmv groups batches of at least
+ * 128 rows (up to 4096 rows, r_max >= 2); the flags override that:
  *   MLORA_LAUNCH_GROUP_ROWS   group (when num_rows <= 4096 and r_max >= 2)
  *   MLORA_LAUNCH_NO_GROUPING  never group
  *   MLORA_LAUNCH_PROGRAMMATIC programmatic dependent launch for the first kernel of the call
