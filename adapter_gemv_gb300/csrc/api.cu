@@ -257,8 +257,21 @@ int run_sgmv(int mode, mlora::DecodeParams &d, const mlora_pool *const *pools, v
     rc = run_tc(mode, d.prob[q], pools[q], d.seg_off, d.seg_slot, d.nseg, d.M, d.status, stream);
   }
   // after a tensor-core launch the CUDA-core kernel needs no early start (no PDL): on the caller's
-  // stream its dependency is that launch; on the side stream, the work before the call
-  if (rc == MLORA_OK) rc = run(mode, pools[0]->dtype, d, side ? side->stream : stream, false);
+  // stream its dependency is that launch; on the side stream, the work before the call. A fused
+  // call on a pool of large ranks (the decode rows of a mixed batch, each on its own adapter)
+  // streams its short segments instead (bgmv_stream.cu).
+  if (rc == MLORA_OK) {
+    cudaStream_t cst = side ? side->stream : st;
+    if (mode == mlora::MODE_FUSED && d.nprob == 1 && d.nseg <= mlora::kStreamMaxSegs &&
+        mlora::stream_eligible(d.prob[0].pool, d.M)) {
+      const cudaError_t e = mlora::launch_sgmv_stream(d.prob[0], d.seg_off, d.seg_slot, d.nseg, d.prob[0].tc_min, d.M,
+                                                      d.status, g_wait_limit_ns, cst);
+      if (e != cudaSuccess) rc = cuda_fail(e, "streaming SGMV launch");
+      else g_launches.fetch_add(1, std::memory_order_relaxed);
+    } else {
+      rc = run(mode, pools[0]->dtype, d, cst, false);
+    }
+  }
   if (side) {  // joined even after an error: nothing is left on the side stream (nor in a capture)
     cudaError_t e = cudaEventRecord(side->joined, side->stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, side->joined, 0);

@@ -67,11 +67,12 @@ constexpr int RSEG = kStreamSegRows;
 //                    reads a slot's page-table entries once, when it checks them)
 //   x                [RSEG][kpad]: the x slices of the segment's rows (one segment at a time)
 //   ring             [stages][32 KB]
+//   (SGMV: [1024, 5124) the first unit of every segment of the call, and the unit count)
 struct Smem {
   int vx, vsm, pt, x, ring, total;
   __host__ __device__ static Smem make(int kpad, int ptn, int stages) {
     Smem s;
-    s.vx = 1024;
+    s.vx = 1024 + (kStreamMaxSegs + 1) * 4;
     s.vsm = s.vx + RQ * MAX_CS * RSEG * MAX_RANK * 4;
     s.pt = s.vsm + RSEG * MAX_RANK * 4;
     s.x = (s.pt + RQ * ptn * 4 + 127) & ~127;
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
   const int cs = p.cs, NS = p.stages;
   const int c = cs > 1 ? (int)cluster_ctarank() : 0;
   const int cb = (int)blockIdx.x / cs, C = (int)gridDim.x / cs;  // this cluster, the clusters
-  const int nseg = p.segs[0];                                     // written by the plan kernel
+  int32_t *ufirst = reinterpret_cast<int32_t *>(smem + 1024);     // SGMV: [nseg + 1]
   // this CTA's slices of d_in and d_out
   const int k0 = min(c * p.kc, pl.d_in), k1 = min(k0 + p.kc, pl.d_in);
   const int n0 = min(c * p.nc, pl.d_out), n1 = min(n0 + p.nc, pl.d_out);
@@ -150,6 +151,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
     *stop = 0;
     mbar_fence_init();
   }
+  // The units of work: BGMV, the plan kernel's segments; SGMV, the pieces of at most RSEG rows of
+  // the segments shorter than tc_min (warp 0 counts them and checks the offsets, as the decode
+  // kernel does: a malformed list is reported and nothing is done).
+  if (p.seg_off != nullptr && warp == 0) {
+    const int per = (p.nseg + 32) / 32;  // segments per lane, (nseg + 1) entries in all
+    int32_t cnt = 0, bad = 0;
+    for (int q = lane * per; q < min((lane + 1) * per, p.nseg); ++q) {
+      const int32_t a = p.seg_off[q], b = p.seg_off[q + 1], len = b - a;
+      bad |= (len < 0) | (a < 0) | (b > p.M);
+      cnt += (len > 0 && len < p.tc_min) ? (len + RSEG - 1) / RSEG : 0;
+    }
+    if (lane == 0) bad |= p.nseg > 0 ? (p.seg_off[0] != 0) | (p.seg_off[p.nseg] != p.M) : (p.M != 0);
+    int32_t incl = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    int32_t run = incl - cnt;
+    for (int q = lane * per; q < min((lane + 1) * per, p.nseg); ++q) {
+      ufirst[q] = run;
+      const int32_t len = p.seg_off[q + 1] - p.seg_off[q];
+      run += (len > 0 && len < p.tc_min) ? (len + RSEG - 1) / RSEG : 0;
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 31) ufirst[p.nseg] = bad ? 0 : incl;
+    if (bad && lane == 0 && blockIdx.x == 0) report(p.status, MLORA_STATUS_BAD_OFFSETS);
+  }
+  __syncthreads();
+  const int nseg = p.seg_off != nullptr ? ufirst[p.nseg] : p.segs[0];  // units
   // x past the slice is zero (the copies write [0, k1 - k0) of each row only): a chunk's tail then
   // adds nothing, whatever stale bytes its stage holds (those are masked on the A side too)
   for (int e = (k1 - k0) + tid * 8; e < p.kpad; e += NTHREADS * 8)
@@ -170,9 +201,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
       const uint32_t use = (uint32_t)(i / RQ);
       ok = __all_sync(0xffffffffu, (use == 0 || mbar_wait(&segempty[q], (use - 1) & 1u, wlim)) && !*stop);
       if (!ok) break;
-      const int t0 = p.segs[1 + sg], t1 = sg + 1 < nseg ? p.segs[2 + sg] : p.M;
+      int t0, t1, s;
+      if (p.seg_off != nullptr) {  // the segment holding unit sg (the last whose first unit is <= sg) and its piece
+        int lo = 0, hi = p.nseg;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (ufirst[mid] <= sg) lo = mid;
+          else hi = mid;
+        }
+        t0 = p.seg_off[lo] + (sg - ufirst[lo]) * RSEG;
+        t1 = min(p.seg_off[lo + 1], t0 + RSEG);
+        s = p.seg_slot[lo];
+      } else {
+        t0 = p.segs[1 + sg];
+        t1 = sg + 1 < nseg ? p.segs[2 + sg] : p.M;
+        s = p.sslot[t0];
+      }
       const int nrows = t1 - t0;  // 1..RSEG rows sharing one slot
-      const int32_t s = p.sslot[t0];
       int32_t rank = 0, bad = 0;
       float scale = 0.f;
       if (s >= 0 && s < pl.num_slots) {
@@ -201,7 +246,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
       }
       const bool valid = s >= 0 && !bad;
       int32_t row = 0;
-      if (lane < nrows) row = p.perm[t0 + lane];
+      if (lane < nrows) row = p.seg_off != nullptr ? t0 + lane : p.perm[t0 + lane];
       if (lane < RSEG) desc[q].rows[lane] = row;
       if (lane == 0) {
         desc[q].nrows = nrows;
@@ -464,23 +509,17 @@ bool stream_eligible(const PoolDev &pool, int num_rows) {
   return ptn <= bstream::MAX_PT && bstream::Smem::make(kpad, ptn, 2).total <= 227 * 1024;
 }
 
-cudaError_t launch_bgmv_stream(const ProblemDev &pr, const int32_t *perm, const int32_t *sslot, const int32_t *segs,
-                               int32_t M, int32_t *status, uint64_t wait_ns, cudaStream_t stream) {
+static cudaError_t launch_stream(StreamParams p, cudaStream_t stream) {
   using namespace bstream;
-  StreamParams p{};
-  p.pr = pr;
-  p.perm = perm;
-  p.sslot = sslot;
-  p.segs = segs;
-  p.M = M;
-  p.status = status;
-  p.wait_ns = wait_ns;
+  const ProblemDev &pr = p.pr;
+  const int32_t M = p.M;
   p.cs = stream_ctas(pr.pool);
   p.kc = ((pr.pool.d_in + p.cs - 1) / p.cs + 7) & ~7;
   p.nc = ((pr.pool.d_out + p.cs - 1) / p.cs + 7) & ~7;
   p.kpad = (p.kc + CHUNK - 1) / CHUNK * CHUNK;
   p.ptn = pr.pool.kind == MLORA_POOL_PAGED ? pr.pool.r_max * (pr.pool.a_ppv + pr.pool.b_ppv) : 0;
-  if (p.ptn > MAX_PT || pr.pool.r_max > MAX_RANK) return cudaErrorInvalidValue;
+  if (p.ptn > MAX_PT || pr.pool.r_max > MAX_RANK || (p.seg_off != nullptr && p.nseg > kStreamMaxSegs))
+    return cudaErrorInvalidValue;
   const int fixed = Smem::make(p.kpad, p.ptn, 0).total;
   int stages = (227 * 1024 - fixed) / STAGE_BYTES;
   stages = stages > MAX_STAGES ? MAX_STAGES : stages;
@@ -515,6 +554,33 @@ cudaError_t launch_bgmv_stream(const ProblemDev &pr, const int32_t *perm, const 
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3((unsigned)(clusters * p.cs), 1, 1);
   return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_bgmv_stream(const ProblemDev &pr, const int32_t *perm, const int32_t *sslot, const int32_t *segs,
+                               int32_t M, int32_t *status, uint64_t wait_ns, cudaStream_t stream) {
+  StreamParams p{};
+  p.pr = pr;
+  p.perm = perm;
+  p.sslot = sslot;
+  p.segs = segs;
+  p.M = M;
+  p.status = status;
+  p.wait_ns = wait_ns;
+  return launch_stream(p, stream);
+}
+
+cudaError_t launch_sgmv_stream(const ProblemDev &pr, const int32_t *seg_off, const int32_t *seg_slot, int32_t nseg,
+                               int32_t tc_min, int32_t M, int32_t *status, uint64_t wait_ns, cudaStream_t stream) {
+  StreamParams p{};
+  p.pr = pr;
+  p.seg_off = seg_off;
+  p.seg_slot = seg_slot;
+  p.nseg = nseg;
+  p.tc_min = tc_min;
+  p.M = M;
+  p.status = status;
+  p.wait_ns = wait_ns;
+  return launch_stream(p, stream);
 }
 
 }  // namespace mlora

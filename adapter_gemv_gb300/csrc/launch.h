@@ -108,8 +108,12 @@ cudaError_t launch_bgmv_plan(const int32_t *row_slot, int32_t M, const PoolDev &
 constexpr int kStreamSegRows = 4;  // rows per segment at most
 struct StreamParams {
   ProblemDev pr;
-  const int32_t *perm, *sslot;  // the grouped order (bgmv_plan.cu)
-  const int32_t *segs;          // [0]: segment count, [1 + k]: first position of segment k
+  const int32_t *perm, *sslot;  // BGMV: the grouped order (bgmv_plan.cu)
+  const int32_t *segs;          // BGMV: [0] segment count, [1 + k] first position of segment k
+  // SGMV (seg_off != nullptr): the call's segments; those shorter than tc_min rows are this
+  // kernel's (the longer ones go to the tensor-core kernels), cut into pieces of kStreamSegRows
+  const int32_t *seg_off, *seg_slot;
+  int32_t nseg, tc_min;
   int32_t M;
   int32_t *status;
   uint64_t wait_ns;
@@ -122,6 +126,11 @@ struct StreamParams {
 bool stream_eligible(const PoolDev &pool, int num_rows);
 cudaError_t launch_bgmv_stream(const ProblemDev &pr, const int32_t *perm, const int32_t *sslot, const int32_t *segs,
                                int32_t M, int32_t *status, uint64_t wait_ns, cudaStream_t stream);
+// The short segments of an SGMV call whose long segments the tensor-core kernels take (at most
+// kStreamMaxSegs segments).
+constexpr int kStreamMaxSegs = 1024;
+cudaError_t launch_sgmv_stream(const ProblemDev &pr, const int32_t *seg_off, const int32_t *seg_slot, int32_t nseg,
+                               int32_t tc_min, int32_t M, int32_t *status, uint64_t wait_ns, cudaStream_t stream);
 
 // CUDA-core path for decode-sized tiles (decode_launch.cu chooses the split and the stages;
 // decode_{shrink,expand,fused}.cu hold the kernels). force_csplit > 0 overrides the split.

@@ -188,8 +188,9 @@ def test_paged_hetero_rank_70b(dev, mode):
 def test_mixed_prefill_decode_13b_sampled(dev):
     """The bench's mixed batch (Punica's batch layout: 3 prompts of 300-2000 rows, then 64 one-row
     decode segments on their own adapters; Llama-2-13B shapes, r = 64), all 7 projections through
-    the fused call: the prompts on the tensor cores, the decode rows on the CUDA-core kernel. The
-    oracle checks every decode row and rows at both sides of every prompt's 128-row blocks."""
+    the fused call: the prompts on the tensor cores, the decode rows streamed on the CUDA cores
+    (one cluster per row). The oracle checks every decode row and rows at both sides of every
+    prompt's 128-row blocks."""
     w = W.mixed_prefill_decode_13b(device=dev)
     off = w.batch.seg_offsets.cpu().numpy()
     rows = np.unique(np.r_[prefill_sample_rows(W.Batch(int(off[3]), w.batch.row_slot[:off[3]],
