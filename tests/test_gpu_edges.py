@@ -404,3 +404,79 @@ def test_bgmv_row_grouping_status_contract(dev):
     good = slots.cpu().clone()
     good[[1, 2, 3, 4, 8, 11]] = -1
     check_op(op, W.Batch(12, good.to(dev), None, None), "bgmv", y, what="valid rows, grouped")
+
+
+def test_streaming_status_contract(dev):
+    """The streaming kernel (grouped BGMV rows on a pool of r_max >= 32, and the short segments of a
+    fused SGMV call whose long segments take the tensor cores): the same status bits as the oracle
+    for bad slots, ranks, page ids and offsets; affected rows untouched bit for bit; other rows
+    correct."""
+    dt = torch.bfloat16
+    rng = np.random.default_rng(31)
+    g = W.generator(31, dev)
+    S, M = 6, 300
+    ranks = np.array([32, 8, 17, 32, 1, 24], np.int32)
+    pool = W.paged_pool(num_slots=S, num_layers=1, r_max=32, d_in=256, d_out=200, dtype=dt, gen=g, device=dev, rng=rng,
+                        ranks=ranks, page_elems=128)
+    x = W.normal((M, 256), 1.0, dt, g, dev)
+    y0 = W.uniform((M, 200), -1, 1, dt, g, dev)
+    op_pool = oracle_pool(pool)
+
+    def both(form, meta, rank=None, a_tab=None):
+        rk = pool.rank if rank is None else rank
+        at = pool.a_page_table if a_tab is None else a_tab
+        p2 = W.Pool(dt, S, 1, 32, 256, 200, rk, pool.scale, pages=pool.pages, a_page_table=at,
+                    b_page_table=pool.b_page_table)
+        h = m.make_pool(p2)
+        y = y0.clone()
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        before = m.launch_count()
+        if form == "sgmv":
+            off, ss = meta
+            m.lora_sgmv(y, x, h, off.to(dev), ss.to(dev), 0, new_v(M, 32, dev), st)
+        else:
+            m.lora_bgmv_ex(y, x, h, meta.to(dev), 0, new_v(M, 32, dev), m.LAUNCH_GROUP_ROWS, st)
+        torch.cuda.synchronize()
+        assert m.launch_count() - before == (3 if form == "sgmv" else 2)
+        opool = oracle.Pool(dtype=odt(dt), num_slots=S, num_layers=1, r_max=32, d_in=256, d_out=200,
+                            rank=rk.cpu().numpy(), scale=pool.scale.cpu().numpy(), pages=op_pool.pages,
+                            a_page_table=at.cpu().numpy(), b_page_table=pool.b_page_table.cpu().numpy())
+        if form == "sgmv":
+            yo, _, _, so = oracle.sgmv(opool, 0, bits(x), bits(y0), meta[0].numpy(), meta[1].numpy())
+        else:
+            yo, _, _, so = oracle.bgmv(opool, 0, bits(x), bits(y0), meta.numpy())
+        return bits(y), yo, int(st.item()), so
+
+    t = lambda a: torch.tensor(a, dtype=torch.int32)
+    # BGMV: slots with repeats (segments of several rows), -1 rows, slots past the pool
+    slots = rng.integers(0, S, M).astype(np.int32)
+    slots[::7] = -1
+    slots[3::11] = 9
+    slots[5::13] = -4
+    gb, ob, sg, so = both("bgmv", t(slots))
+    assert sg == so == m.STATUS_BAD_SLOT
+    bad = (slots < 0) | (slots >= S)
+    assert np.array_equal(gb[bad], bits(y0)[bad])
+    assert_close(oracle.decode(gb[~bad], odt(dt)), oracle.decode(ob[~bad], odt(dt)), "streamed bgmv, valid rows")
+    # a rank out of range, then a page id out of range
+    rk = pool.rank.clone()
+    rk[2] = 0
+    s2 = np.tile(np.arange(S, dtype=np.int32), M // S)
+    gb, ob, sg, so = both("bgmv", t(s2), rank=rk)
+    assert sg == so == m.STATUS_BAD_RANK and np.array_equal(gb[s2 == 2], bits(y0)[s2 == 2])
+    at = pool.a_page_table.clone()
+    at[3, 0, 5, 1] = pool.pages.shape[0]
+    gb, ob, sg, so = both("bgmv", t(s2), a_tab=at)
+    assert sg == so == m.STATUS_BAD_PAGE and np.array_equal(gb[s2 == 3], bits(y0)[s2 == 3])
+    ok = (s2 != 3)
+    assert_close(oracle.decode(gb[ok], odt(dt)), oracle.decode(ob[ok], odt(dt)), "bad page, other rows")
+    # SGMV: a long segment on the tensor cores, short ones streamed, one short segment on a bad slot
+    off, ss = t([0, 260, 265, 266, 269, 300]), t([0, 1, 9, 3, 5])
+    gs, os_, sg, so = both("sgmv", (off, ss))
+    assert sg == so == m.STATUS_BAD_SLOT and np.array_equal(gs[265:266], bits(y0)[265:266])
+    keep = np.r_[0:265, 266:300]
+    assert_close(oracle.decode(gs[keep], odt(dt)), oracle.decode(os_[keep], odt(dt)), "streamed sgmv, valid rows")
+    # malformed offsets: nothing written, the bit reported
+    for bad_off in ([0, 260, 250, 269, 280, 300], [0, 260, 265, 266, 269, 299]):
+        gs, os_, sg, so = both("sgmv", (t(bad_off), ss))
+        assert sg == so == m.STATUS_BAD_OFFSETS and np.array_equal(gs, bits(y0))
