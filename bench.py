@@ -663,14 +663,14 @@ def run_reference(args):
 REFERENCE_BUDGET_S = 120.0
 
 
-NCU_TARGETS = ("decode7b", "decode7b-2layers", "decode7b-identical-2layers", "q_proj", "prefill13b-q", "paged70b")
+NCU_TARGETS = ("decode7b", "decode7b-2layers", "decode7b-identical-2layers", "q_proj", "prefill13b-q", "paged70b", "paged70b-ungrouped")
 
 
 def run_ncu_target(name: str, reps: int):
     """Run one workload `reps` times with no timing, as a target for ncu (nothing is printed but
     'ok'). decode7b-2layers is the decode step with 2 layers: the same launches per layer, a
     smaller footprint for multi-pass captures; decode7b-identical-2layers the same with every row
-    on one adapter."""
+    on one adapter; paged70b-ungrouped the paged 70B batch with no row grouping."""
     import adapter_gemv_gb300 as m
     from adapter_gemv_gb300.plan import StepPlan
     dev = torch.device("cuda", 0)
@@ -694,13 +694,14 @@ def run_ncu_target(name: str, reps: int):
         v = torch.empty((w.batch.M, op.pool.r_max), dtype=torch.float32, device=dev)
         for _ in range(reps):
             m.lora_sgmv(op.y, op.x, h, w.batch.seg_offsets, w.batch.seg_slot, 0, v)
-    elif name == "paged70b":
+    elif name.startswith("paged70b"):
         w = W.paged_decode_70b(device=dev)
         op = w.ops[0]
         h = m.make_pool(op.pool)
         v = torch.empty((w.batch.M, op.pool.r_max), dtype=torch.float32, device=dev)
+        fl = m.LAUNCH_NO_GROUPING if name.endswith("ungrouped") else 0
         for _ in range(reps):
-            m.lora_bgmv(op.y, op.x, h, w.batch.row_slot, 0, v)
+            m.lora_bgmv_ex(op.y, op.x, h, w.batch.row_slot, 0, v, fl)
     torch.cuda.synchronize()
     print("ok", name)
 
