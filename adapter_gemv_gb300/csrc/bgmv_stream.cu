@@ -63,18 +63,21 @@ constexpr int RSEG = kStreamSegRows;
 //   [512, 1024)      RQ segment descriptors and the stop flag
 //   vx               [RQ][MAX_CS][RSEG][MAX_RANK] fp32: partial v of every CTA of the cluster
 //   vsm              [RSEG][MAX_RANK] fp32: the summed v
+//   red              [gmax][CWARPS][32] fp32: the consumer warps' lane sums of every rank-row group
+//                    of the segment (gmax = r_max / 8 rounded up)
 //   pt               [RQ][ptn] int32: page ids of the segments in flight (paged pools: the producer
 //                    reads a slot's page-table entries once, when it checks them)
 //   x                [RSEG][kpad]: the x slices of the segment's rows (one segment at a time)
 //   ring             [stages][32 KB]
 //   (SGMV: [1024, 5124) the first unit of every segment of the call, and the unit count)
 struct Smem {
-  int vx, vsm, pt, x, ring, total;
-  __host__ __device__ static Smem make(int kpad, int ptn, int stages) {
+  int vx, vsm, red, pt, x, ring, total;
+  __host__ __device__ static Smem make(int kpad, int ptn, int stages, int gmax) {
     Smem s;
     s.vx = 1024 + (kStreamMaxSegs + 1) * 4;
     s.vsm = s.vx + RQ * MAX_CS * RSEG * MAX_RANK * 4;
-    s.pt = s.vsm + RSEG * MAX_RANK * 4;
+    s.red = s.vsm + RSEG * MAX_RANK * 4;
+    s.pt = s.red + gmax * CWARPS * 32 * 4;
     s.x = (s.pt + RQ * ptn * 4 + 127) & ~127;
     s.ring = (s.x + RSEG * kpad * 2 + 1023) & ~1023;
     s.total = s.ring + stages * STAGE_BYTES;
@@ -100,6 +103,52 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 
+// Eight products of chunk xv with chunk av (8 packed 16-bit elements each) into one fp32 chain,
+// mixed-precision FMAs (16-bit operands, fp32 accumulator, one rounding per product).
+template <int DT>
+__device__ __forceinline__ void mfma8_chain(const uint4 &xv, const uint4 &av, float &c) {
+  const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, as[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if constexpr (DT == MLORA_BF16)
+      asm("{ .reg .b16 xl, xh, al, ah; mov.b32 {xl, xh}, %1; mov.b32 {al, ah}, %2;\n"
+          " fma.rn.f32.bf16 %0, xl, al, %0; fma.rn.f32.bf16 %0, xh, ah, %0; }"
+          : "+f"(c) : "r"(xs[q]), "r"(as[q]));
+    else
+      asm("{ .reg .b16 xl, xh, al, ah; mov.b32 {xl, xh}, %1; mov.b32 {al, ah}, %2;\n"
+          " fma.rn.f32.f16 %0, xl, al, %0; fma.rn.f32.f16 %0, xh, ah, %0; }"
+          : "+f"(c) : "r"(xs[q]), "r"(as[q]));
+  }
+}
+
+// Sums of N values (N = 8, 16 or 32) over the 32 lanes of a warp, scattered over the lanes: each
+// butterfly step halves the values a lane keeps (the lanes with the step's bit set keep the upper
+// half and send the lower), so after the halving steps lane l holds the sum of value l / (32 / N)
+// (the remaining steps add across the lanes that share it). 31 shuffles for N = 32, against
+// 160 for a full reduction of every value.
+template <int N>
+__device__ __forceinline__ float lane_sum_scatter(float (&v)[N], int lane) {
+  constexpr int H = N == 32 ? 5 : N == 16 ? 4 : 3;
+  static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 values");
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int sft = 16 >> st;
+    if (st < H) {
+      const int n = N >> st;
+      const bool up = (lane & sft) != 0;
+#pragma unroll
+      for (int k = 0; k < n / 2; ++k) {
+        const float send = up ? v[k] : v[k + n / 2];
+        const float keep = up ? v[k + n / 2] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
+      }
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], sft);
+    }
+  }
+  return v[0];
+}
+
 // Unit i of cluster b of C in snake order.
 __device__ __forceinline__ int snake(int i, int b, int C) { return i * C + ((i & 1) ? C - 1 - b : b); }
 
@@ -116,7 +165,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
   uint64_t *xempty = xfull + 1;                          // the consumers are done with the x slices
   SegDesc *desc = reinterpret_cast<SegDesc *>(smem + 512);
   volatile int32_t *stop = reinterpret_cast<volatile int32_t *>(smem + 512 + RQ * sizeof(SegDesc));
-  const Smem S = Smem::make(p.kpad, p.ptn, p.stages);
+  const Smem S = Smem::make(p.kpad, p.ptn, p.stages, (p.pr.pool.r_max + ROWS - 1) / ROWS);
   float *vx = reinterpret_cast<float *>(smem + S.vx);
   float *vsm = reinterpret_cast<float *>(smem + S.vsm);
   uint16_t *xbuf = reinterpret_cast<uint16_t *>(smem + S.x);
@@ -347,48 +396,65 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
         ++xuse;
         if (cs > 1 && tid == 0) mbar_arrive_expect_tx(&vfull[q], (uint32_t)((cs - 1) * nrows * rank * 4));
         float *vmine = vx + (q * MAX_CS + c) * RSEG * MAX_RANK;  // [RSEG][MAX_RANK]
+        // Warp w owns the 16-byte pieces w * 32 + lane of every chunk: it loads each row's x piece
+        // once per stage into registers and dots it with the piece of each of the stage's rank-rows
+        // (one fp32 chain per rank-row and row). After the group's last chunk the chains are summed
+        // over the lanes (scattered: lane l keeps value l / (32 / N)) into the group's slot in shared
+        // memory; once every group is in, the warps' sums are added in warp order. No barrier
+        // couples the warps inside the loop.
+        constexpr int N = ROWS * R;  // values per lane: index jj * R + r
         for (int g = 0; g < groups && ok; ++g) {
-          const int j = g * ROWS + warp;
-          float c0[R], c1[R];
+          const int nr8 = min(ROWS, rank - g * ROWS);
+          float acc[N];
   #pragma unroll
-          for (int r = 0; r < R; ++r) c0[r] = c1[r] = 0.f;
-          for (int ch = 0; ch < kchunks; ++ch) {
+          for (int k = 0; k < N; ++k) acc[k] = 0.f;
+          for (int ch = 0; ch < kchunks && ok; ++ch) {
             const int slot = (int)(ctr % NS);
             if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (ctr / NS) & 1u, wlim) && !*stop)) {
               ok = false;
               break;
             }
-            if (j < rank) {
-              const int e0 = ch * CHUNK, len8 = min(CHUNK, k1 - k0 - e0) >> 3;
-              const uint16_t *ar = reinterpret_cast<const uint16_t *>(ring + (size_t)slot * STAGE_BYTES) + warp * CHUNK;
+            const int e0 = ch * CHUNK, len8 = min(CHUNK, k1 - k0 - e0) >> 3;
+            const int c8 = warp * 32 + lane;  // 16-byte pieces, consecutive across the lanes
+            if (c8 < len8) {
+              uint4 xr[R];
   #pragma unroll
-              for (int u = 0; u < CHUNK / 256; ++u) {
-                const int c8 = u * 32 + lane;  // 16-byte pieces, consecutive across the lanes
-                const uint4 av = c8 < len8 ? *reinterpret_cast<const uint4 *>(ar + c8 * 8) : make_uint4(0u, 0u, 0u, 0u);
+              for (int r = 0; r < R; ++r)
+                xr[r] = r < nrows ? *reinterpret_cast<const uint4 *>(xbuf + r * p.kpad + e0 + c8 * 8) : make_uint4(0u, 0u, 0u, 0u);
+              const uint16_t *ar = reinterpret_cast<const uint16_t *>(ring + (size_t)slot * STAGE_BYTES) + c8 * 8;
   #pragma unroll
-                for (int r = 0; r < R; ++r)
-                  if (r < nrows) mfma8<DT>(*reinterpret_cast<const uint4 *>(xbuf + r * p.kpad + e0 + c8 * 8), av, c0[r], c1[r]);
+              for (int jj = 0; jj < ROWS; ++jj) {
+                if (jj < nr8) {
+                  const uint4 av = *reinterpret_cast<const uint4 *>(ar + jj * CHUNK);
+  #pragma unroll
+                  for (int r = 0; r < R; ++r)
+                    if (r < nrows) mfma8_chain<DT>(xr[r], av, acc[jj * R + r]);
+                }
               }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
             ++ctr;
           }
-          if (ok && j < rank) {
-  #pragma unroll
-            for (int r = 0; r < R; ++r) {
-              if (r < nrows) {
-                float v = c0[r] + c1[r];
-  #pragma unroll
-                for (int sft = 16; sft > 0; sft >>= 1) v += __shfl_xor_sync(0xffffffffu, v, sft);
-                // this CTA's partial into slot c of every CTA's exchange buffer
-                if (lane == 0) {
-                  vmine[r * MAX_RANK + j] = v;
-                  for (int pe = 1; pe < cs; ++pe) {
-                    const uint32_t peer = (uint32_t)((c + pe) % cs);
-                    st_async_f32(dsmem_addr(vmine + r * MAX_RANK + j, peer), v, dsmem_addr(&vfull[q], peer));
-                  }
-                }
+          if (ok) {
+            const float tot = lane_sum_scatter<N>(acc, lane);
+            float *red = reinterpret_cast<float *>(smem + S.red) + g * CWARPS * 32;
+            if ((lane & (32 / N - 1)) == 0) red[warp * 32 + lane / (32 / N)] = tot;
+          }
+        }
+        ok = !consumers_or(!ok);  // every group's sums are in (or some warp gave up)
+        if (ok) {
+          const float *red = reinterpret_cast<const float *>(smem + S.red);
+          for (int e = tid; e < groups * N; e += CWARPS * 32) {
+            const int g = e / N, k = e % N, jj = k / R, r = k % R, j = g * ROWS + jj;
+            if (j < rank && r < nrows) {
+              float v = 0.f;
+              for (int w = 0; w < CWARPS; ++w) v += red[(g * CWARPS + w) * 32 + k];
+              // this CTA's partial into slot c of every CTA's exchange buffer
+              vmine[r * MAX_RANK + j] = v;
+              for (int pe = 1; pe < cs; ++pe) {
+                const uint32_t peer = (uint32_t)((c + pe) % cs);
+                st_async_f32(dsmem_addr(vmine + r * MAX_RANK + j, peer), v, dsmem_addr(&vfull[q], peer));
               }
             }
           }
@@ -506,7 +572,8 @@ bool stream_eligible(const PoolDev &pool, int num_rows) {
   const int kc = ((pool.d_in + cs - 1) / cs + 7) & ~7;
   const int kpad = (kc + bstream::CHUNK - 1) / bstream::CHUNK * bstream::CHUNK;
   const int ptn = pool.kind == MLORA_POOL_PAGED ? pool.r_max * (pool.a_ppv + pool.b_ppv) : 0;
-  return ptn <= bstream::MAX_PT && bstream::Smem::make(kpad, ptn, 2).total <= 227 * 1024;
+  return ptn <= bstream::MAX_PT &&
+         bstream::Smem::make(kpad, ptn, 2, (pool.r_max + bstream::ROWS - 1) / bstream::ROWS).total <= 227 * 1024;
 }
 
 static cudaError_t launch_stream(StreamParams p, cudaStream_t stream) {
@@ -520,12 +587,13 @@ static cudaError_t launch_stream(StreamParams p, cudaStream_t stream) {
   p.ptn = pr.pool.kind == MLORA_POOL_PAGED ? pr.pool.r_max * (pr.pool.a_ppv + pr.pool.b_ppv) : 0;
   if (p.ptn > MAX_PT || pr.pool.r_max > MAX_RANK || (p.seg_off != nullptr && p.nseg > kStreamMaxSegs))
     return cudaErrorInvalidValue;
-  const int fixed = Smem::make(p.kpad, p.ptn, 0).total;
+  const int gmax = (pr.pool.r_max + ROWS - 1) / ROWS;
+  const int fixed = Smem::make(p.kpad, p.ptn, 0, gmax).total;
   int stages = (227 * 1024 - fixed) / STAGE_BYTES;
   stages = stages > MAX_STAGES ? MAX_STAGES : stages;
   if (stages < 2) return cudaErrorInvalidConfiguration;
   p.stages = stages;
-  const size_t smem = (size_t)Smem::make(p.kpad, p.ptn, stages).total;
+  const size_t smem = (size_t)Smem::make(p.kpad, p.ptn, stages, gmax).total;
   auto kern = pr.pool.dtype == MLORA_BF16 ? stream_kernel<MLORA_BF16> : stream_kernel<MLORA_FP16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
