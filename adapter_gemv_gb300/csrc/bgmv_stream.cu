@@ -15,9 +15,11 @@
 //     rows), publishes it in a descriptor and issues the bulk copies: the slices of the segment's x
 //     rows, then the stages -- a stage is 8 rank-rows x 2048 elements (32 KB): A^T's row groups for
 //     every chunk of the d_in slice, then B's row groups for every chunk of the d_out slice;
-//   * eight consumer warps: for an A stage, warp w dots rank-row 8g + w's chunk with every row's x
-//     chunk (mixed-precision FMAs, fp32 sums, two chains per lane) and sums its lanes after the
-//     group's last chunk (Punica section 3.4, the shrink, split over d_in); the cluster's partial
+//   * eight consumer warps: for an A stage, warp w dots its 256-element slice of each of the
+//     stage's 8 rank-rows with every row's x slice, held in registers (mixed-precision FMAs, one
+//     fp32 chain per rank-row and row), and after the group's last chunk sums the chains over its
+//     lanes into shared memory; the warps' sums are added in warp order once per segment (Punica
+//     section 3.4, the shrink, split over d_in); the cluster's partial
 //     sums are pushed into every peer's shared memory (st.async, completing on the receiver's
 //     mbarrier) and summed in CTA-rank order; for a B stage, thread t accumulates its 8 columns of
 //     every row over the group's rank-rows (paired fp32 FMAs) and, after the chunk's last group,
