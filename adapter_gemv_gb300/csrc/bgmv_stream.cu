@@ -13,9 +13,10 @@
 // keeps up to 128 KB in flight whatever the rank and never reloads operands from L2 after a wait:
 //   * one producer warp per CTA resolves each segment (slot, rank, scale, page ids, checked; the
 //     rows), publishes it in a descriptor and issues the bulk copies: the slices of the segment's x
-//     rows, then the stages -- a stage is 8 rank-rows x 2048 elements (32 KB): A^T's row groups for
-//     every chunk of the d_in slice, then B's row groups for every chunk of the d_out slice;
-//   * eight consumer warps: for an A stage, warp w dots its 256-element slice of each of the
+//     rows, then the stages -- a stage is 64 KB: A^T's groups of 8 rank-rows x 4096 elements for
+//     every chunk of the d_in slice, then B's groups of 16 rank-rows x 2048 columns for every chunk
+//     of the d_out slice (a stage's handoff costs about as much for 32 KB as for 64 KB);
+//   * eight consumer warps: for an A stage, warp w dots its two 256-element slices of each of the
 //     stage's 8 rank-rows with every row's x slice, held in registers (mixed-precision FMAs, one
 //     fp32 chain per rank-row and row), and after the group's last chunk sums the chains over its
 //     lanes into shared memory; the warps' sums are added in warp order once per segment (Punica
@@ -44,9 +45,12 @@ namespace bstream {
 
 constexpr int CWARPS = 8;                    // consumer warps
 constexpr int NTHREADS = (CWARPS + 1) * 32;  // + the producer warp
-constexpr int ROWS = 8;                      // rank-rows per stage
-constexpr int CHUNK = 2048;                  // elements of each rank-row per stage
-constexpr int STAGE_BYTES = ROWS * CHUNK * 2;
+constexpr int ROWS = 8;                      // A^T stages: rank-rows per stage
+constexpr int ACHUNK = 4096;                 //             elements of each rank-row per stage
+constexpr int BROWS = 16;                    // B stages: rank-rows per stage
+constexpr int CHUNK = 2048;                  //           columns of each rank-row per stage
+constexpr int STAGE_BYTES = ROWS * ACHUNK * 2;  // 64 KB: the handoffs of a stage cost as much for 32 KB
+static_assert(BROWS * CHUNK == ROWS * ACHUNK, "A^T and B stages of one size");
 constexpr int RQ = 2;                        // segments in flight (descriptors, exchange buffers)
 constexpr int MAX_STAGES = 8;
 constexpr int MAX_RANK = 128;
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
   // this CTA's slices of d_in and d_out
   const int k0 = min(c * p.kc, pl.d_in), k1 = min(k0 + p.kc, pl.d_in);
   const int n0 = min(c * p.nc, pl.d_out), n1 = min(n0 + p.nc, pl.d_out);
-  const int kchunks = (k1 - k0 + CHUNK - 1) / CHUNK, nchunks = (n1 - n0 + CHUNK - 1) / CHUNK;
+  const int kchunks = (k1 - k0 + ACHUNK - 1) / ACHUNK, nchunks = (n1 - n0 + CHUNK - 1) / CHUNK;
   const uint64_t wlim = p.wait_ns ? p.wait_ns : kWaitLimitNs;
 
   if (tid == 0) {
@@ -318,10 +322,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
       ++xuse;
       // the y rows' slices into L2, for the consumers' loads at the start of each chunk
       if (lane < nrows && n1 > n0) prefetch_l2(pr.y + (int64_t)row * pr.ldy + n0, (uint32_t)(n1 - n0) * 2);
-      const int groups = (rank + ROWS - 1) / ROWS;
-      // this segment's stages: A^T (group-major, then d_in chunks), then B (d_out chunks, then groups)
+      const int groups = (rank + ROWS - 1) / ROWS, bgroups = (rank + BROWS - 1) / BROWS;
+      // this segment's stages: A^T (groups of 8 rank-rows, then d_in chunks of 4096), then B (d_out
+      // chunks of 2048, then groups of 16 rank-rows)
       for (int ph = 0; ph < 2 && ok; ++ph) {
-        const int outer = ph == 0 ? groups : nchunks, inner = ph == 0 ? kchunks : groups;
+        const int outer = ph == 0 ? groups : nchunks, inner = ph == 0 ? kchunks : bgroups;
+        const int srows = ph == 0 ? ROWS : BROWS, schunk = ph == 0 ? ACHUNK : CHUNK;
         for (int o = 0; o < outer && ok; ++o) {
           for (int in = 0; in < inner; ++in) {
             const int g = ph == 0 ? o : in, ch = ph == 0 ? in : o;
@@ -329,13 +335,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
             const uint32_t su = ctr / NS;
             ok = __all_sync(0xffffffffu, (su == 0 || mbar_wait(&empty[slot], (su - 1) & 1u, wlim)) && !*stop);
             if (!ok) break;
-            const int e0 = (ph == 0 ? k0 : n0) + ch * CHUNK;
-            const int len = min(CHUNK, (ph == 0 ? k1 : n1) - e0), nr8 = min(ROWS, rank - g * ROWS);
+            const int e0 = (ph == 0 ? k0 : n0) + ch * schunk;
+            const int len = min(schunk, (ph == 0 ? k1 : n1) - e0), nr8 = min(srows, rank - g * srows);
             if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(nr8 * len * 2));
             __syncwarp();
             if (lane < nr8) {
-              uint16_t *dst = reinterpret_cast<uint16_t *>(ring + (size_t)slot * STAGE_BYTES) + lane * CHUNK;
-              const int j = g * ROWS + lane;
+              uint16_t *dst = reinterpret_cast<uint16_t *>(ring + (size_t)slot * STAGE_BYTES) + lane * schunk;
+              const int j = g * srows + lane;
               if (ph == 0)
                 decode::vec_pieces<true>(pl, s, pr.layer, j, e0, e0 + len, a_tr, [&](const uint16_t *src, int off, int n) {
                   bulk_g2s_hint(dst + off, src, (uint32_t)n * 2, &full[slot], pol);
@@ -398,8 +404,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
         ++xuse;
         if (cs > 1 && tid == 0) mbar_arrive_expect_tx(&vfull[q], (uint32_t)((cs - 1) * nrows * rank * 4));
         float *vmine = vx + (q * MAX_CS + c) * RSEG * MAX_RANK;  // [RSEG][MAX_RANK]
-        // Warp w owns the 16-byte pieces w * 32 + lane of every chunk: it loads each row's x piece
-        // once per stage into registers and dots it with the piece of each of the stage's rank-rows
+        // Warp w owns the 16-byte pieces 256 u + 32 w + lane (u = 0, 1) of every 4096-element chunk:
+        // it loads each row's x pieces once per stage into registers and dots them with the pieces
+        // of each of the stage's rank-rows
         // (one fp32 chain per rank-row and row). After the group's last chunk the chains are summed
         // over the lanes (scattered: lane l keeps value l / (32 / N)) into the group's slot in shared
         // memory; once every group is in, the warps' sums are added in warp order. No barrier
@@ -416,21 +423,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
               ok = false;
               break;
             }
-            const int e0 = ch * CHUNK, len8 = min(CHUNK, k1 - k0 - e0) >> 3;
-            const int c8 = warp * 32 + lane;  // 16-byte pieces, consecutive across the lanes
-            if (c8 < len8) {
-              uint4 xr[R];
+            const int e0 = ch * ACHUNK, len8 = min(ACHUNK, k1 - k0 - e0) >> 3;
   #pragma unroll
-              for (int r = 0; r < R; ++r)
-                xr[r] = r < nrows ? *reinterpret_cast<const uint4 *>(xbuf + r * p.kpad + e0 + c8 * 8) : make_uint4(0u, 0u, 0u, 0u);
-              const uint16_t *ar = reinterpret_cast<const uint16_t *>(ring + (size_t)slot * STAGE_BYTES) + c8 * 8;
+            for (int u = 0; u < ACHUNK / 2048; ++u) {
+              const int c8 = u * 256 + warp * 32 + lane;  // 16-byte pieces, consecutive across the lanes
+              if (c8 < len8) {
+                uint4 xr[R];
   #pragma unroll
-              for (int jj = 0; jj < ROWS; ++jj) {
-                if (jj < nr8) {
-                  const uint4 av = *reinterpret_cast<const uint4 *>(ar + jj * CHUNK);
+                for (int r = 0; r < R; ++r)
+                  xr[r] = r < nrows ? *reinterpret_cast<const uint4 *>(xbuf + r * p.kpad + e0 + c8 * 8) : make_uint4(0u, 0u, 0u, 0u);
+                const uint16_t *ar = reinterpret_cast<const uint16_t *>(ring + (size_t)slot * STAGE_BYTES) + c8 * 8;
   #pragma unroll
-                  for (int r = 0; r < R; ++r)
-                    if (r < nrows) mfma8_chain<DT>(xr[r], av, acc[jj * R + r]);
+                for (int jj = 0; jj < ROWS; ++jj) {
+                  if (jj < nr8) {
+                    const uint4 av = *reinterpret_cast<const uint4 *>(ar + jj * ACHUNK);
+  #pragma unroll
+                    for (int r = 0; r < R; ++r)
+                      if (r < nrows) mfma8_chain<DT>(xr[r], av, acc[jj * R + r]);
+                  }
                 }
               }
             }
@@ -492,13 +502,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
           for (int r = 0; r < R; ++r)
   #pragma unroll
             for (int e = 0; e < 4; ++e) acc[r][e] = make_float2(0.f, 0.f);
-          for (int g = 0; g < groups; ++g) {
+          const int bgroups = (rank + BROWS - 1) / BROWS;
+          for (int g = 0; g < bgroups; ++g) {
             const int slot = (int)(ctr % NS);
             if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (ctr / NS) & 1u, wlim) && !*stop)) {
               ok = false;
               break;
             }
-            const int nr8 = min(ROWS, rank - g * ROWS);
+            const int nr8 = min(BROWS, rank - g * BROWS);
             if (mine) {
               const uint16_t *br = reinterpret_cast<const uint16_t *>(ring + (size_t)slot * STAGE_BYTES) + tid * 8;
               for (int w = 0; w < nr8; ++w) {
@@ -507,7 +518,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(const __grid_consta
   #pragma unroll
                 for (int r = 0; r < R; ++r) {
                   if (r < nrows) {
-                    const float vj = vsm[r * MAX_RANK + g * ROWS + w];
+                    const float vj = vsm[r * MAX_RANK + g * BROWS + w];
                     const float2 v2 = make_float2(vj, vj);
   #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[r][e] = __ffma2_rn(v2, b2[e], acc[r][e]);
