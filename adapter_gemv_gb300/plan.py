@@ -15,6 +15,20 @@ import torch
 from . import MLORA_MAX_GROUP, CallSequence, Group, make_pool
 
 
+def group_ops(ops: Sequence) -> List[List]:
+    """Consecutive ops of one layer that read the same x (same storage) and whose pools share a
+    dtype, at most MLORA_MAX_GROUP at a time, in step order: the problems of one grouped call."""
+    groups: List[List] = []
+    for op in ops:
+        g = groups[-1] if groups else None
+        if (g and len(g) < MLORA_MAX_GROUP and g[0].layer == op.layer
+                and g[0].x.data_ptr() == op.x.data_ptr() and g[0].pool.dtype == op.pool.dtype):
+            g.append(op)
+        else:
+            groups.append([op])
+    return groups
+
+
 class StepPlan:
     def __init__(self, ops: Sequence, batch, status=None, programmatic: bool = True):
         """ops: objects with .pool .layer .x .y (as workloads.Op); batch: .M .seg_offsets .seg_slot.
@@ -24,14 +38,7 @@ class StepPlan:
         pool). The first call keeps an ordinary dependency on whatever ran before the step."""
         self.programmatic = programmatic
         self.handles = {}
-        groups: List[List] = []
-        for op in ops:
-            g = groups[-1] if groups else None
-            if (g and len(g) < MLORA_MAX_GROUP and g[0].layer == op.layer
-                    and g[0].x.data_ptr() == op.x.data_ptr() and g[0].pool.dtype == op.pool.dtype):
-                g.append(op)
-            else:
-                groups.append([op])
+        groups = group_ops(ops)
         dev = ops[0].x.device
         r_max = max(op.pool.r_max for op in ops)
         width = max(len(g) for g in groups)
